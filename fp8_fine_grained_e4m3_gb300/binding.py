@@ -1,0 +1,219 @@
+"""ctypes binding over libfp8gemm.so (include/fp8gemm.h).
+
+Argument marshalling only: every function here checks tensor metadata,
+allocates outputs with torch when the caller gives none, and passes raw
+device pointers plus the current CUDA stream to the C ABI.  All arithmetic
+runs in the library's kernels.  There is no fallback: if the library is
+missing or a call fails, an exception is raised.
+
+FP8 operands are uint8 tensors holding e4m3 bytes (a torch.float8_e4m3fn
+tensor is accepted and viewed as uint8); scales are float32; outputs are
+bfloat16.
+"""
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+OK = 0
+ERR_NULL = -1
+ERR_ALIGN = -2
+ERR_SHAPE = -3
+ERR_ARCH = -4
+ERR_LAUNCH = -5
+ERR_DEVICE_STATUS = -6
+ERR_TIMEOUT = -7
+
+_lib = None
+_lock = threading.Lock()
+
+# (name, restype, argtypes) for every entry point of include/fp8gemm.h
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+SIGNATURES = [
+    ("fp8_quant_1x128", _I, [_P, _P, _P, _I, _I, _P]),
+    ("fp8_quant_128x128", _I, [_P, _P, _P, _I, _I, _I, _P]),
+    ("fp8gemm_dense", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _P]),
+    ("fp8gemm_grouped_contiguous", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
+    ("fp8gemm_grouped_masked", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
+    ("fp8gemm_get_device_status", _I, [_P, ctypes.POINTER(ctypes.c_int)]),
+    ("fp8gemm_strerror", ctypes.c_char_p, [_I]),
+    ("fp8gemm_num_kernel_launches", ctypes.c_uint64, []),
+]
+
+
+class FP8GemmError(RuntimeError):
+    def __init__(self, code, where):
+        self.code = code
+        super().__init__(f"{where}: {strerror(code)} (code {code})")
+
+
+def library_path():
+    return _build.LIB_PATH
+
+
+def lib():
+    """Load libfp8gemm.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        with _lock:
+            if _lib is None:
+                path = library_path()
+                if not os.path.exists(path):
+                    raise RuntimeError(
+                        f"{path} is missing: build it first "
+                        "(python -c 'import __graft_entry__ as g; g.build()')")
+                L = ctypes.CDLL(path)
+                for name, res, args in SIGNATURES:
+                    f = getattr(L, name)
+                    f.restype = res
+                    f.argtypes = args
+                _lib = L
+    return _lib
+
+
+def strerror(code: int) -> str:
+    return lib().fp8gemm_strerror(int(code)).decode()
+
+
+def num_kernel_launches() -> int:
+    return int(lib().fp8gemm_num_kernel_launches())
+
+
+def _check(code, where):
+    if code != OK:
+        raise FP8GemmError(code, where)
+
+
+# ----------------------------------------------------------------- helpers
+def _torch():
+    import torch
+    return torch
+
+
+def _stream(stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _u8(t, name):
+    torch = _torch()
+    if t.dtype == torch.float8_e4m3fn:
+        t = t.view(torch.uint8)
+    if t.dtype != torch.uint8:
+        raise TypeError(f"{name} must hold e4m3 bytes (uint8 or float8_e4m3fn), got {t.dtype}")
+    return _dev(t, name)
+
+
+def _f32(t, name):
+    if t.dtype != _torch().float32:
+        raise TypeError(f"{name} must be float32, got {t.dtype}")
+    return _dev(t, name)
+
+
+def _i32(t, name):
+    if t.dtype != _torch().int32:
+        raise TypeError(f"{name} must be int32, got {t.dtype}")
+    return _dev(t, name)
+
+
+def _dev(t, name):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+# ------------------------------------------------------------ entry points
+def fp8_quant_1x128(X, Q=None, sX=None, stream=None):
+    """X f32 [..., K] -> (Q u8 [..., K], sX f32 [..., K/128]).  Leading dims are
+    flattened into M."""
+    torch = _torch()
+    X = _f32(X, "X")
+    K = X.shape[-1]
+    M = X.numel() // K if K else 0
+    if Q is None:
+        Q = torch.empty(X.shape, dtype=torch.uint8, device=X.device)
+    if sX is None:
+        sX = torch.empty((*X.shape[:-1], max(K // 128, 0)), dtype=torch.float32, device=X.device)
+    _check(lib().fp8_quant_1x128(_ptr(X), _ptr(_u8(Q, "Q")), _ptr(_f32(sX, "sX")), M, K,
+                                 _stream(stream)), "fp8_quant_1x128")
+    return Q, sX
+
+
+def fp8_quant_128x128(W, Q=None, sW=None, stream=None):
+    """W f32 [N, K] or [E, N, K] -> (Q u8 same shape, sW f32 [(E,) ceil(N/128), K/128])."""
+    torch = _torch()
+    W = _f32(W, "W")
+    squeeze = W.dim() == 2
+    W3 = W.unsqueeze(0) if squeeze else W
+    E, N, K = W3.shape
+    if Q is None:
+        Q = torch.empty(W.shape, dtype=torch.uint8, device=W.device)
+    if sW is None:
+        shp = ((N + 127) // 128, K // 128)
+        sW = torch.empty(shp if squeeze else (E, *shp), dtype=torch.float32, device=W.device)
+    _check(lib().fp8_quant_128x128(_ptr(W3), _ptr(_u8(Q, "Q")), _ptr(_f32(sW, "sW")), E, N, K,
+                                   _stream(stream)), "fp8_quant_128x128")
+    return Q, sW
+
+
+def fp8gemm_dense(A, sA, B, sB, D=None, stream=None):
+    """A u8 [M, K], sA [M, K/128], B u8 [N, K], sB [ceil(N/128), K/128] -> D bf16 [M, N]."""
+    torch = _torch()
+    A, B = _u8(A, "A"), _u8(B, "B")
+    M, K = A.shape
+    N = B.shape[0]
+    if D is None:
+        D = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    _check(lib().fp8gemm_dense(_ptr(A), _ptr(_f32(sA, "sA")), _ptr(B), _ptr(_f32(sB, "sB")),
+                               _ptr(_dev(D, "D")), M, N, K, _stream(stream)), "fp8gemm_dense")
+    return D
+
+
+def fp8gemm_grouped_contiguous(A, sA, B, sB, m_indices, D=None, stream=None):
+    """A u8 [M_pad, K], B u8 [E, N, K], m_indices i32 [M_pad] -> D bf16 [M_pad, N]."""
+    torch = _torch()
+    A, B = _u8(A, "A"), _u8(B, "B")
+    M_pad, K = A.shape
+    E, N = B.shape[0], B.shape[1]
+    if D is None:
+        D = torch.empty((M_pad, N), dtype=torch.bfloat16, device=A.device)
+    _check(lib().fp8gemm_grouped_contiguous(
+        _ptr(A), _ptr(_f32(sA, "sA")), _ptr(B), _ptr(_f32(sB, "sB")),
+        _ptr(_i32(m_indices, "m_indices")), _ptr(_dev(D, "D")), M_pad, N, K, E,
+        _stream(stream)), "fp8gemm_grouped_contiguous")
+    return D
+
+
+def fp8gemm_grouped_masked(A, sA, B, sB, masked_m, D=None, stream=None):
+    """A u8 [E, M_max, K], B u8 [E, N, K], masked_m i32 [E] -> D bf16 [E, M_max, N]
+    (rows >= masked_m[e] are not written)."""
+    torch = _torch()
+    A, B = _u8(A, "A"), _u8(B, "B")
+    E, M_max, K = A.shape
+    N = B.shape[1]
+    if D is None:
+        D = torch.empty((E, M_max, N), dtype=torch.bfloat16, device=A.device)
+    _check(lib().fp8gemm_grouped_masked(
+        _ptr(A), _ptr(_f32(sA, "sA")), _ptr(B), _ptr(_f32(sB, "sB")),
+        _ptr(_i32(masked_m, "masked_m")), _ptr(_dev(D, "D")), E, M_max, N, K,
+        _stream(stream)), "fp8gemm_grouped_masked")
+    return D
+
+
+def fp8gemm_get_device_status(stream=None) -> int:
+    """Synchronise the stream, then read and clear the device status word."""
+    out = ctypes.c_int(0)
+    _check(lib().fp8gemm_get_device_status(_stream(stream), ctypes.byref(out)),
+           "fp8gemm_get_device_status")
+    return out.value

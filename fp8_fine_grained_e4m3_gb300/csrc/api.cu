@@ -1,0 +1,274 @@
+// api.cu -- the C ABI of libfp8gemm.so (declared in include/fp8gemm.h).
+//
+// Every entry point validates its arguments on the host and only then
+// enqueues kernels ("lpnh.cn/news/2822121" section 4.2: do the expensive
+// checking and configuration on the host, so the kernel only loops; section
+// 6.3, first point: TMA wants 16-byte aligned addresses and strides).
+#include <atomic>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "common.cuh"
+
+namespace fp8gemm {
+
+// Per-device status word (one instance per device the library is loaded on).
+__device__ int g_device_status = 0;
+
+namespace {
+
+std::atomic<unsigned long long> g_launches{0};
+
+struct DeviceInfo {
+  int num_sms = 0;
+  int cc_major = 0, cc_minor = 0;
+  int* status = nullptr;
+  bool ok = false;
+};
+
+std::mutex g_mu;
+std::map<int, DeviceInfo> g_devices;
+std::map<std::pair<int, cudaStream_t>, std::pair<void*, size_t>> g_workspaces;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return EncodeTiledFn(nullptr);
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// Looks up (once per device) the SM count, compute capability and the
+// device address of the status word.
+int device_info(DeviceInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FP8GEMM_ERR_LAUNCH;
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_devices.find(dev);
+  if (it == g_devices.end()) {
+    DeviceInfo d;
+    if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) !=
+            cudaSuccess)
+      return FP8GEMM_ERR_LAUNCH;
+    d.ok = d.cc_major == 10 && d.cc_minor == 3;
+    if (d.ok && cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_device_status) !=
+                    cudaSuccess)
+      return FP8GEMM_ERR_LAUNCH;
+    it = g_devices.emplace(dev, d).first;
+  }
+  *out = it->second;
+  return it->second.ok ? FP8GEMM_OK : FP8GEMM_ERR_ARCH;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int finish(cudaError_t e, int nlaunch) {
+  if (e != cudaSuccess) {
+    cudaGetLastError();  // clear the sticky-free launch error
+    return FP8GEMM_ERR_LAUNCH;
+  }
+  g_launches += nlaunch;
+  return FP8GEMM_OK;
+}
+
+// Workspace for the split-K reduction of the small-M path, one per
+// (device, stream), zero-initialised (its counters must start at 0).
+int workspace_for(cudaStream_t s, size_t bytes, void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FP8GEMM_ERR_LAUNCH;
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto key = std::make_pair(dev, s);
+  auto it = g_workspaces.find(key);
+  if (it != g_workspaces.end() && it->second.second >= bytes) {
+    *out = it->second.first;
+    return FP8GEMM_OK;
+  }
+  if (it != g_workspaces.end()) {  // grow: the old buffer may still be in use on s
+    if (cudaStreamSynchronize(s) != cudaSuccess) return FP8GEMM_ERR_LAUNCH;
+    cudaFree(it->second.first);
+    g_workspaces.erase(it);
+  }
+  void* p = nullptr;
+  if (cudaMalloc(&p, bytes) != cudaSuccess) return FP8GEMM_ERR_LAUNCH;
+  if (cudaMemset(p, 0, bytes) != cudaSuccess) {
+    cudaFree(p);
+    return FP8GEMM_ERR_LAUNCH;
+  }
+  g_workspaces[key] = std::make_pair(p, bytes);
+  *out = p;
+  return FP8GEMM_OK;
+}
+
+constexpr int kSmallM = 64;  // dense calls with M <= this use the swap-AB stream-K kernel
+
+}  // namespace
+
+bool make_tmap_u8_sw128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                        uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || rows == 0 || cols == 0) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols};  // bytes between rows
+  const cuuint32_t box[2] = {uint32_t(kBlockK), box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace fp8gemm
+
+using namespace fp8gemm;
+
+namespace {
+
+// Shared shape rules: K a positive multiple of 128, N a multiple of 8, sizes
+// non-negative, and every byte offset the kernels form within int64 / int32
+// index range.
+int check_common(int M, int N, int K) {
+  if (M < 0 || N < 0 || K < 0) return FP8GEMM_ERR_SHAPE;
+  if (K == 0 || K % kBlockK != 0 || N % 8 != 0) return FP8GEMM_ERR_SHAPE;
+  return FP8GEMM_OK;
+}
+
+int ctx_for(cudaStream_t stream, LaunchCtx* c) {
+  DeviceInfo d;
+  const int r = device_info(&d);
+  if (r != FP8GEMM_OK) return r;
+  c->stream = stream;
+  c->num_sms = d.num_sms;
+  c->status = d.status;
+  return FP8GEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fp8_quant_1x128(const float* X, uint8_t* Q, float* sX, int M, int K,
+                    fp8gemm_stream_t stream) {
+  if (M < 0 || K < 0 || K % kBlockK != 0) return FP8GEMM_ERR_SHAPE;
+  if (M == 0 || K == 0) return FP8GEMM_OK;
+  if (!X || !Q || !sX) return FP8GEMM_ERR_NULL;
+  if (!aligned16(X) || !aligned16(Q) || !aligned16(sX)) return FP8GEMM_ERR_ALIGN;
+  LaunchCtx c;
+  if (int r = ctx_for(stream, &c)) return r;
+  return finish(launch_quant_1x128(c, X, Q, sX, M, K), 1);
+}
+
+int fp8_quant_128x128(const float* W, uint8_t* Q, float* sW, int E, int N, int K,
+                      fp8gemm_stream_t stream) {
+  if (E < 0 || N < 0 || K < 0 || K % kBlockK != 0) return FP8GEMM_ERR_SHAPE;
+  if (E == 0 || N == 0 || K == 0) return FP8GEMM_OK;
+  if ((long long)E * N * (long long)K > (1LL << 46)) return FP8GEMM_ERR_SHAPE;
+  if (!W || !Q || !sW) return FP8GEMM_ERR_NULL;
+  if (!aligned16(W) || !aligned16(Q) || !aligned16(sW)) return FP8GEMM_ERR_ALIGN;
+  LaunchCtx c;
+  if (int r = ctx_for(stream, &c)) return r;
+  return finish(launch_quant_128x128(c, W, Q, sW, E, N, K), 1);
+}
+
+int fp8gemm_dense(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB, void* D,
+                  int M, int N, int K, fp8gemm_stream_t stream) {
+  if (int r = check_common(M, N, K)) return r;
+  if (M == 0 || N == 0) return FP8GEMM_OK;
+  if (!A || !sA || !B || !sB || !D) return FP8GEMM_ERR_NULL;
+  if (!aligned16(A) || !aligned16(sA) || !aligned16(B) || !aligned16(sB) || !aligned16(D))
+    return FP8GEMM_ERR_ALIGN;
+  LaunchCtx c;
+  if (int r = ctx_for(stream, &c)) return r;
+  GemmArgs a{GemmMode::kDense, A, sA, B, sB, nullptr, static_cast<__nv_bfloat16*>(D),
+             M, N, K, 1};
+  if (M <= kSmallM) {
+    const size_t bytes = small_m_workspace_bytes(c.num_sms, N);
+    void* ws = nullptr;
+    if (int r = workspace_for(stream, bytes, &ws)) return r;
+    return finish(launch_gemm_small_m(c, a, ws, bytes), 1);
+  }
+  return finish(launch_gemm_tc(c, a), 1);
+}
+
+int fp8gemm_grouped_contiguous(const uint8_t* A, const float* sA, const uint8_t* B,
+                               const float* sB, const int32_t* m_indices, void* D, int M_pad,
+                               int N, int K, int E, fp8gemm_stream_t stream) {
+  if (int r = check_common(M_pad, N, K)) return r;
+  if (E < 0 || M_pad % kBlockM != 0) return FP8GEMM_ERR_SHAPE;
+  if ((long long)E * N > 0x7fffffffLL) return FP8GEMM_ERR_SHAPE;
+  if (M_pad == 0 || N == 0 || E == 0) return FP8GEMM_OK;
+  if (!A || !sA || !B || !sB || !m_indices || !D) return FP8GEMM_ERR_NULL;
+  if (!aligned16(A) || !aligned16(sA) || !aligned16(B) || !aligned16(sB) ||
+      !aligned16(m_indices) || !aligned16(D))
+    return FP8GEMM_ERR_ALIGN;
+  LaunchCtx c;
+  if (int r = ctx_for(stream, &c)) return r;
+  GemmArgs a{GemmMode::kContiguous, A, sA, B, sB, m_indices, static_cast<__nv_bfloat16*>(D),
+             M_pad, N, K, E};
+  return finish(launch_gemm_tc(c, a), 1);
+}
+
+int fp8gemm_grouped_masked(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                           const int32_t* masked_m, void* D, int E, int M_max, int N, int K,
+                           fp8gemm_stream_t stream) {
+  if (int r = check_common(M_max, N, K)) return r;
+  if (E < 0) return FP8GEMM_ERR_SHAPE;
+  if ((long long)E * M_max > 0x7fffffffLL || (long long)E * N > 0x7fffffffLL)
+    return FP8GEMM_ERR_SHAPE;
+  if (M_max == 0 || N == 0 || E == 0) return FP8GEMM_OK;
+  if (!A || !sA || !B || !sB || !masked_m || !D) return FP8GEMM_ERR_NULL;
+  if (!aligned16(A) || !aligned16(sA) || !aligned16(B) || !aligned16(sB) ||
+      !aligned16(masked_m) || !aligned16(D))
+    return FP8GEMM_ERR_ALIGN;
+  LaunchCtx c;
+  if (int r = ctx_for(stream, &c)) return r;
+  GemmArgs a{GemmMode::kMasked, A, sA, B, sB, masked_m, static_cast<__nv_bfloat16*>(D),
+             M_max, N, K, E};
+  return finish(launch_gemm_tc(c, a), 1);
+}
+
+int fp8gemm_get_device_status(fp8gemm_stream_t stream, int* out) {
+  if (!out) return FP8GEMM_ERR_NULL;
+  DeviceInfo d;
+  if (int r = device_info(&d)) return r;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return FP8GEMM_ERR_LAUNCH;
+  int v = 0;
+  if (cudaMemcpy(&v, d.status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return FP8GEMM_ERR_LAUNCH;
+  const int zero = 0;
+  if (cudaMemcpy(d.status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+    return FP8GEMM_ERR_LAUNCH;
+  *out = v;
+  return FP8GEMM_OK;
+}
+
+const char* fp8gemm_strerror(int code) {
+  switch (code) {
+    case FP8GEMM_OK: return "ok";
+    case FP8GEMM_ERR_NULL: return "a required pointer is NULL";
+    case FP8GEMM_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+    case FP8GEMM_ERR_SHAPE: return "unsupported shape (K % 128, N % 8, M_pad % 128, sign or range)";
+    case FP8GEMM_ERR_ARCH: return "current device is not compute capability 10.3 (sm_103a)";
+    case FP8GEMM_ERR_LAUNCH: return "CUDA launch or runtime call failed";
+    case FP8GEMM_ERR_DEVICE_STATUS: return "device-side input error (expert index or row count)";
+    case FP8GEMM_ERR_TIMEOUT: return "a pipeline wait exceeded its time limit";
+    default: return "unknown status";
+  }
+}
+
+uint64_t fp8gemm_num_kernel_launches(void) { return g_launches.load(); }
+
+}  // extern "C"

@@ -1,0 +1,66 @@
+// common.cuh -- definitions shared by the kernels and the host launcher.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/fp8gemm.h"
+
+namespace fp8gemm {
+
+constexpr int kBlockK = 128;  // K block of the scaling granularity (= 128 e4m3 bytes)
+constexpr int kBlockM = 128;  // rows per tile (= TMEM lanes)
+constexpr float kE4M3Max = 448.0f;
+
+// Kernels report device-side conditions through a per-device status word
+// (first error wins); the host passes its address to every launch.
+__device__ __forceinline__ void raise_status(int* status, int code) {
+  atomicCAS(status, 0, code);
+}
+
+__host__ __device__ constexpr int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// ------------------------------------------------------------ launch hooks
+// Each kernel file exposes one host function that launches its kernels; the
+// C ABI in api.cu validates arguments and then calls these.
+
+struct LaunchCtx {
+  cudaStream_t stream;
+  int num_sms;
+  int* status;  // device address of the status word
+};
+
+cudaError_t launch_quant_1x128(const LaunchCtx& c, const float* X, uint8_t* Q, float* sX,
+                               int M, int K);
+cudaError_t launch_quant_128x128(const LaunchCtx& c, const float* W, uint8_t* Q, float* sW,
+                                 int E, int N, int K);
+
+// Problem description for the persistent tensor-core GEMM.
+enum class GemmMode : int { kDense = 0, kContiguous = 1, kMasked = 2 };
+
+struct GemmArgs {
+  GemmMode mode;
+  const uint8_t* A;
+  const float* sA;
+  const uint8_t* B;
+  const float* sB;
+  const int32_t* group_info;  // m_indices (contiguous) or masked_m (masked)
+  __nv_bfloat16* D;
+  int M;      // dense: M; contiguous: M_pad; masked: M_max (rows per expert)
+  int N, K;
+  int E;      // experts (1 for dense)
+};
+
+cudaError_t launch_gemm_tc(const LaunchCtx& c, const GemmArgs& a);
+cudaError_t launch_gemm_small_m(const LaunchCtx& c, const GemmArgs& a, void* workspace,
+                                size_t workspace_bytes);
+size_t small_m_workspace_bytes(int num_sms, int N);
+
+// Encodes a 2-D K-major uint8 tensor map with 128-byte swizzling:
+// rows x cols bytes, box of box_rows x 128 bytes.  Defined in api.cu.
+bool make_tmap_u8_sw128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                        uint32_t box_rows);
+
+}  // namespace fp8gemm

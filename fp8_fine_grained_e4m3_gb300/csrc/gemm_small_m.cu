@@ -1,0 +1,354 @@
+// gemm_small_m.cu -- the dense FP8 block-scaled GEMM for decode-sized M
+// (M <= 64), where the weights dominate the bytes moved.
+//
+// Same arithmetic as gemm_tc.cu (per-K-block tensor-core partial, promoted
+// with sA[m, kb] * sB[n/128, kb] into FP32, BF16 out), laid out for small M:
+//
+// * Swap AB: the weight tile (128 rows of B) is the MMA's M operand and the
+//   M <= 64 activation rows, padded to MP in {16, 32, 64}, are its N operand,
+//   so the 128-lane MMA is filled by weights instead of by padding.  TMEM lane
+//   = output column n, TMEM column = output row m.
+// * Stream-K: the (N tile, K block) units are dealt out evenly over one CTA
+//   per SM, so every SM streams the same number of weight bytes even when
+//   N/128 is far below the SM count ("news.rkmt.cn/news/5092" sections 1.2
+//   and 4.2: with M of 1-16, fixed tiles leave most SMs idle; size the work
+//   to the SM count).  A CTA whose range ends inside a tile leaves its FP32
+//   partial in a workspace slot; the last CTA to finish a tile (atomic
+//   counter) sums every contributor's partial in CTA order -- a fixed order,
+//   so the result is deterministic -- writes BF16 and resets the counter.
+//
+// CTA layout (192 threads): warps 0-3 promotion/epilogue (thread = TMEM lane
+// = output column), warp 4 TMA producer, warp 5 MMA issuer.
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace fp8gemm {
+namespace {
+
+constexpr int kSmStages = 8;
+constexpr int kCounterBytes = 256 * 1024;  // one int per N tile: N <= 8M columns
+constexpr int kMaxMP = 64;
+
+template <int MP_>
+struct SmCfg {
+  static constexpr int MP = MP_;
+  static constexpr int kStages = kSmStages;
+  static constexpr int kThreads = 192;
+  static constexpr int kTmaWarp = 4;
+  static constexpr int kMmaWarp = 5;
+  static constexpr int kWBytes = 128 * kBlockK;  // weight tile: 16 KB
+  static constexpr int kXBytes = MP * kBlockK;   // activation tile
+  static constexpr int kTmemCols = 2 * MP < 32 ? 32 : 2 * MP;
+  static constexpr int kAuxBytes = 1024;
+  static constexpr size_t kSmemBytes =
+      1024 + size_t(kStages) * (kWBytes + kXBytes) + kAuxBytes;
+  static_assert(MP == 16 || MP == 32 || MP == 64, "MP");
+};
+
+struct StreamK {
+  long long U;  // units = tiles * Kb
+  int G, Kb;
+  __device__ long long begin(int c) const { return (long long)c * U / G; }
+  __device__ int cta_of(long long u) const { return int(((u + 1) * G - 1) / U); }
+};
+
+__device__ __forceinline__ void drain_wait_sm(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > 200000000ull) break;
+  }
+}
+
+template <class Cfg>
+__global__ void __launch_bounds__(Cfg::kThreads, 1)
+    gemm_small_m_kernel(const __grid_constant__ CUtensorMap tmW,
+                        const __grid_constant__ CUtensorMap tmX, const GemmArgs args,
+                        float* ws_partials, int* ws_counters, int* status) {
+  constexpr int MP = Cfg::MP;
+  constexpr int kStages = Cfg::kStages;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smW = smem;
+  uint8_t* smX = smem + kStages * Cfg::kWBytes;
+  uint8_t* aux = smX + kStages * Cfg::kXBytes;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(aux);
+  uint64_t* empty_bar = full_bar + kStages;
+  uint64_t* tfull_bar = full_bar + 2 * kStages;
+  uint64_t* tempty_bar = full_bar + 2 * kStages + 2;
+  uint64_t* drain_bar = full_bar + 2 * kStages + 4;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(full_bar + 2 * kStages + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_holder + 2);
+  uint64_t* group_bar = full_bar + 2 * kStages + 7;
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int Kb = args.K / kBlockK;
+  const int n_tiles = ceil_div(args.N, 128);
+  StreamK sk{(long long)n_tiles * Kb, int(gridDim.x), Kb};
+  const long long u_begin = sk.begin(blockIdx.x);
+  const long long u_end = sk.begin(blockIdx.x + 1);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull_bar[b], 1);
+      mbar_init(&tempty_bar[b], 4);
+    }
+    mbar_init(drain_bar, 1);
+    mbar_init(group_bar, 128);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == Cfg::kMmaWarp) {
+    tmem_alloc(tmem_holder, Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == Cfg::kTmaWarp && lane == 0) {
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmX);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  auto fail = [&]() {
+    *abort_flag = 1;
+    raise_status(status, FP8GEMM_ERR_TIMEOUT);
+  };
+
+  if (warp == Cfg::kTmaWarp) {
+    if (lane == 0) {
+      const uint64_t pol_stream = l2_policy_evict_first();  // weights: read once
+      const uint64_t pol_keep = l2_policy_evict_last();     // activations: read by all
+      uint32_t it = 0;
+      bool ok = true;
+      for (long long u = u_begin; u < u_end && ok;) {
+        const int tile = int(u / Kb);
+        const int kb0 = int(u % Kb);
+        const int kb1 = int(min((long long)Kb, kb0 + (u_end - u)));
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          const int s = it % kStages;
+          const uint32_t ph = (it / kStages) & 1;
+          if (!mbar_wait(&empty_bar[s], ph ^ 1, abort_flag)) {
+            fail();
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full_bar[s], Cfg::kWBytes + Cfg::kXBytes);
+          tma_load_2d_hint(smW + s * Cfg::kWBytes, &tmW, &full_bar[s], kb * kBlockK, tile * 128,
+                           pol_stream);
+          tma_load_2d_hint(smX + s * Cfg::kXBytes, &tmX, &full_bar[s], kb * kBlockK, 0,
+                           pol_keep);
+        }
+        u += kb1 - kb0;
+      }
+      const uint32_t n = it < uint32_t(kStages) ? it : uint32_t(kStages);
+      for (uint32_t i = it - n; i < it; ++i)
+        drain_wait_sm(&full_bar[i % kStages], (i / kStages) & 1);
+    }
+  } else if (warp == Cfg::kMmaWarp) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_e4m3_f32(128, MP);
+      const uint32_t w_base = smem_addr(smW);
+      const uint32_t x_base = smem_addr(smX);
+      uint32_t it = 0;
+      bool ok = true;
+      for (long long u = u_begin; u < u_end && ok;) {
+        const int kb0 = int(u % Kb);
+        const int kb1 = int(min((long long)Kb, kb0 + (u_end - u)));
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          const int s = it % kStages;
+          const uint32_t ph = (it / kStages) & 1;
+          const int buf = it & 1;
+          const uint32_t tph = (it >> 1) & 1;
+          if (!mbar_wait(&tempty_bar[buf], tph ^ 1, abort_flag) ||
+              !mbar_wait(&full_bar[s], ph, abort_flag)) {
+            fail();
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + buf * MP;
+#pragma unroll
+          for (int k = 0; k < kBlockK / 32; ++k) {
+            const uint64_t ad = smem_desc_sw128_kmajor(w_base + s * Cfg::kWBytes + k * 32);
+            const uint64_t bd = smem_desc_sw128_kmajor(x_base + s * Cfg::kXBytes + k * 32);
+            umma_e4m3(d_tmem, ad, bd, idesc, k > 0 ? 1u : 0u);
+          }
+          umma_commit(&empty_bar[s]);
+          umma_commit(&tfull_bar[buf]);
+        }
+        u += kb1 - kb0;
+      }
+      if (it > 0) {
+        umma_commit(drain_bar);
+        drain_wait_sm(drain_bar, 0);
+      }
+    }
+  } else {
+    // -------------------------------------------- promotion + epilogue
+    const int t = threadIdx.x;  // TMEM lane = column within the N tile
+    const uint32_t lane_base = uint32_t(warp * 32) << 16;
+    const int M = args.M;
+    const int first_tile = int(u_begin / Kb);
+    uint32_t it = 0;
+    uint32_t gphase = 0;
+    bool ok = true;
+    // bounded barrier over the 128 promotion threads
+    auto group_sync = [&]() -> bool {
+      mbar_arrive(group_bar);
+      const bool r = mbar_wait(group_bar, gphase, abort_flag);
+      gphase ^= 1;
+      return r;
+    };
+    for (long long u = u_begin; u < u_end && ok;) {
+      const int tile = int(u / Kb);
+      const int kb0 = int(u % Kb);
+      const int kb1 = int(min((long long)Kb, kb0 + (u_end - u)));
+      const float* sb_ptr = args.sB + size_t(tile) * Kb;
+
+      float acc[MP];
+#pragma unroll
+      for (int j = 0; j < MP; ++j) acc[j] = 0.f;
+
+      for (int kb = kb0; kb < kb1; ++kb, ++it) {
+        // scale product of column j (activation row j) for this K block; the
+        // loads are warp-uniform broadcasts
+        float sc[MP];
+        const float sb = __ldg(sb_ptr + kb);
+#pragma unroll
+        for (int j = 0; j < MP; ++j) sc[j] = j < M ? __ldg(args.sA + size_t(j) * Kb + kb) * sb : 0.f;
+        const int buf = it & 1;
+        const uint32_t tph = (it >> 1) & 1;
+        if (!mbar_wait(&tfull_bar[buf], tph, abort_flag)) {
+          fail();
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + lane_base + buf * MP;
+        if constexpr (MP == 16) {
+          uint32_t r[16];
+          tmem_ld_32x32b_x16(taddr, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) acc[j] = fmaf(__uint_as_float(r[j]), sc[j], acc[j]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < MP / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(taddr + c * 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              acc[c * 32 + j] = fmaf(__uint_as_float(r[j]), sc[c * 32 + j], acc[c * 32 + j]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty_bar[buf]);
+      }
+      if (!ok) break;
+
+      const int n = tile * 128 + t;
+      const bool col_ok = n < args.N;
+      bool write = true;
+      if (!(kb0 == 0 && kb1 == Kb)) {
+        // split tile: publish this CTA's partial, the last contributor reduces
+        const int slot_idx = 2 * blockIdx.x + (tile == first_tile ? 0 : 1);
+        float* mine = ws_partials + size_t(slot_idx) * MP * 128;
+#pragma unroll
+        for (int j = 0; j < MP; ++j) mine[j * 128 + t] = acc[j];
+        __threadfence();
+        if (!group_sync()) { fail(); ok = false; break; }
+        const int c_first = sk.cta_of((long long)tile * Kb);
+        const int c_last = sk.cta_of((long long)(tile + 1) * Kb - 1);
+        if (t == 0) {
+          __threadfence();
+          const int prev = atomicAdd(ws_counters + tile, 1);
+          const int is_last = prev == c_last - c_first;
+          if (is_last) ws_counters[tile] = 0;  // ready for the next launch
+          *last_flag = is_last;
+        }
+        if (!group_sync()) { fail(); ok = false; break; }
+        write = *last_flag != 0;
+        if (!group_sync()) { fail(); ok = false; break; }  // last_flag is reused
+        if (write) {
+          __threadfence();
+#pragma unroll
+          for (int j = 0; j < MP; ++j) acc[j] = 0.f;
+          for (int c = c_first; c <= c_last; ++c) {
+            const int cs = int(sk.begin(c) / Kb) == tile ? 2 * c : 2 * c + 1;
+            const float* p = ws_partials + size_t(cs) * MP * 128;
+#pragma unroll
+            for (int j = 0; j < MP; ++j) acc[j] += __ldcg(p + j * 128 + t);
+          }
+        }
+      }
+      if (write && col_ok) {
+#pragma unroll
+        for (int j = 0; j < MP; ++j)
+          if (j < M) args.D[size_t(j) * args.N + n] = __float2bfloat16_rn(acc[j]);
+      }
+      u += kb1 - kb0;
+    }
+  }
+
+  __syncthreads();
+  if (warp == Cfg::kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+template <class Cfg>
+cudaError_t run(const LaunchCtx& c, const GemmArgs& a, void* ws, size_t ws_bytes) {
+  const int Kb = a.K / kBlockK;
+  const int n_tiles = ceil_div(a.N, 128);
+  const long long U = (long long)n_tiles * Kb;
+  const int grid = int(U < c.num_sms ? U : c.num_sms);
+  if (grid == 0) return cudaSuccess;
+  if (size_t(n_tiles) * 4 > size_t(kCounterBytes) ||
+      ws_bytes < size_t(kCounterBytes) + size_t(2) * grid * Cfg::MP * 128 * 4)
+    return cudaErrorInvalidValue;
+  CUtensorMap tmW, tmX;
+  if (!make_tmap_u8_sw128(&tmW, a.B, uint64_t(a.N), a.K, 128)) return cudaErrorInvalidValue;
+  if (!make_tmap_u8_sw128(&tmX, a.A, uint64_t(a.M), a.K, Cfg::MP)) return cudaErrorInvalidValue;
+  auto kern = gemm_small_m_kernel<Cfg>;
+  static unsigned long long attr_done = 0;  // one bit per device
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!(attr_done >> (dev & 63) & 1ull)) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(Cfg::kSmemBytes));
+    if (e != cudaSuccess) return e;
+    attr_done |= 1ull << (dev & 63);
+  }
+  int* counters = reinterpret_cast<int*>(ws);
+  float* partials = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kCounterBytes);
+  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, c.stream>>>(tmW, tmX, a, partials, counters,
+                                                            c.status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t small_m_workspace_bytes(int num_sms, int /*N*/) {
+  return size_t(kCounterBytes) + size_t(2) * num_sms * kMaxMP * 128 * 4;
+}
+
+cudaError_t launch_gemm_small_m(const LaunchCtx& c, const GemmArgs& a, void* ws,
+                                size_t ws_bytes) {
+  if (a.M <= 16) return run<SmCfg<16>>(c, a, ws, ws_bytes);
+  if (a.M <= 32) return run<SmCfg<32>>(c, a, ws, ws_bytes);
+  return run<SmCfg<64>>(c, a, ws, ws_bytes);
+}
+
+}  // namespace fp8gemm

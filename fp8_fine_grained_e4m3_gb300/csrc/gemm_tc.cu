@@ -1,0 +1,398 @@
+// gemm_tc.cu -- persistent, warp-specialised FP8 block-scaled GEMM on the
+// 5th-generation tensor cores (sm_103a), for the dense and the two MoE
+// grouped forms.
+//
+// What it computes (see include/fp8gemm.h): every 128-wide K block is
+// contracted on the tensor cores into a fresh FP32 partial in TMEM, then
+// "promoted" on the CUDA cores -- multiplied by sA[m, kb] * sB[n/128, kb] and
+// added into an FP32 register accumulator ("lpnh.cn/news/2822121" section 2.3:
+// the scale product changes per K block, so it cannot wait for the end of the
+// K loop; "blog.hotdry.top: DeepGEMM FP8 GEMM fine-grained scaling kernels",
+// section "two-level accumulation": first level on the tensor cores, second
+// level promoted to FP32 on the CUDA cores).  The result is rounded to BF16
+// once, in the epilogue.
+//
+// CTA layout (320 threads, one CTA per SM, persistent over tiles):
+//   warps 0-7  promotion + epilogue: two warpgroups; warpgroup g owns columns
+//              [g*BN/2, (g+1)*BN/2) of the tile, thread = tile row (TMEM lane)
+//   warp 8     TMA producer: A tile 128x128 B and B tile BNx128 B per K block
+//              into a kStages-deep shared-memory ring (128-byte swizzle)
+//   warp 9     MMA issuer (one thread): 4 x tcgen05.mma kind::f8f6f4 (K = 32)
+//              per K block into one of two TMEM partial buffers
+// Synchronisation is by mbarriers only: full/empty per ring stage, and
+// tmem_full/tmem_empty per TMEM buffer, so the tensor cores work on K block
+// kb+1 while the promotion warps drain K block kb.  ("lpnh.cn/news/2822121"
+// sections 3.1-3.3 and 4.1 describe the Hopper form of this pipeline: TMA
+// loads the next block while the matrix instruction consumes the current
+// one, with mbarriers between them.)
+//
+// Tile order: grouped rasterisation (16 M blocks share each sweep over N) so
+// concurrently running CTAs reuse A and B tiles through L2 ("news.rkmt.cn/
+// news/5092" section 3.2: size the work to the SM count).  The masked form
+// enumerates only tiles that hold valid rows, so no CTA idles on an empty
+// expert ("lpnh.cn/news/2822121" section 5.2: skip empty blocks).
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace fp8gemm {
+namespace {
+
+constexpr int kGroupM = 16;  // M blocks per rasterisation group
+
+template <int BN_, int kStages_>
+struct TcCfg {
+  static constexpr int BN = BN_;
+  static constexpr int kStages = kStages_;
+  static constexpr int kPromoWarps = 8;
+  static constexpr int kTmaWarp = 8;
+  static constexpr int kMmaWarp = 9;
+  static constexpr int kThreads = 320;
+  static constexpr int kABytes = kBlockM * kBlockK;  // 16 KB
+  static constexpr int kBBytes = BN * kBlockK;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kColsPerWG = BN / 2;
+  static constexpr int kTmemCols = 2 * BN;  // two partial buffers
+  static constexpr int kBarBytes = 512;
+  static constexpr size_t kSmemBytes = 1024 + size_t(kStages) * kStageBytes + kBarBytes;
+  static_assert(BN == 128 || BN == 256, "BN");
+  static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM columns must be a power of 2");
+};
+
+struct Tile {
+  int row0;        // first row in A's (and D's) 2-D row space
+  int valid_rows;  // rows of this tile that are real outputs
+  int n0;          // first output column
+  int b_row0;      // first row in B's 2-D row space (expert * N + n0)
+  int e;           // expert (0 for dense)
+};
+
+// Walks the same tile sequence in every role of every CTA.
+struct Scheduler {
+  GemmArgs a;
+  int num_m, num_n, Kb, total;
+  int* status;
+
+  __device__ int masked_rows(int e) const {
+    int m = __ldg(a.group_info + e);
+    if (m < 0 || m > a.M) {
+      raise_status(status, FP8GEMM_ERR_DEVICE_STATUS);
+      m = m < 0 ? 0 : a.M;
+    }
+    return m;
+  }
+
+  __device__ void init(const GemmArgs& args, int BN, int* st) {
+    a = args;
+    status = st;
+    Kb = a.K / kBlockK;
+    num_n = ceil_div(a.N, BN);
+    if (a.mode == GemmMode::kMasked) {
+      num_m = ceil_div(a.M, kBlockM);
+      int t = 0;
+      for (int e = 0; e < a.E; ++e) t += ceil_div(masked_rows(e), kBlockM) * num_n;
+      total = t;
+    } else {
+      num_m = ceil_div(a.M, kBlockM);
+      total = num_m * num_n;
+    }
+  }
+
+  // Returns false when the tile holds no work (contiguous padding block or a
+  // bad expert index).
+  __device__ bool get(int t, int BN, Tile& tile) const {
+    if (a.mode == GemmMode::kMasked) {
+      int e = 0;
+      int mb_e = 0;
+      for (; e < a.E; ++e) {
+        mb_e = ceil_div(masked_rows(e), kBlockM);
+        const int cnt = mb_e * num_n;
+        if (t < cnt) break;
+        t -= cnt;
+      }
+      const int mb = t % mb_e;
+      const int nb = t / mb_e;
+      tile.e = e;
+      tile.row0 = e * a.M + mb * kBlockM;
+      tile.valid_rows = min(kBlockM, masked_rows(e) - mb * kBlockM);
+      tile.n0 = nb * BN;
+      tile.b_row0 = e * a.N + tile.n0;
+      return true;
+    }
+    const int per_group = kGroupM * num_n;
+    const int g = t / per_group;
+    const int first_m = g * kGroupM;
+    const int gs = min(kGroupM, num_m - first_m);
+    const int r = t - g * per_group;
+    const int mb = first_m + r % gs;
+    const int nb = r / gs;
+    tile.row0 = mb * kBlockM;
+    tile.n0 = nb * BN;
+    if (a.mode == GemmMode::kContiguous) {
+      const int e = __ldg(a.group_info + tile.row0);
+      if (e < 0) return false;
+      if (e >= a.E) {
+        raise_status(status, FP8GEMM_ERR_DEVICE_STATUS);
+        return false;
+      }
+      tile.e = e;
+      tile.valid_rows = kBlockM;
+      tile.b_row0 = e * a.N + tile.n0;
+      return true;
+    }
+    tile.e = 0;
+    tile.valid_rows = min(kBlockM, a.M - tile.row0);
+    tile.b_row0 = tile.n0;
+    return true;
+  }
+};
+
+// Bounded wait on an mbarrier whose phases may already be complete, with no
+// abort check: used only to let in-flight async copies land before exit.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > 200000000ull) break;
+  }
+}
+
+template <class Cfg>
+__global__ void __launch_bounds__(Cfg::kThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+                   const __grid_constant__ CUtensorMap tmB, const GemmArgs args, int* status) {
+  constexpr int BN = Cfg::BN;
+  constexpr int kStages = Cfg::kStages;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smA = smem;
+  uint8_t* smB = smem + kStages * Cfg::kABytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * Cfg::kStageBytes);
+  uint64_t* full_bar = bars;
+  uint64_t* empty_bar = bars + kStages;
+  uint64_t* tfull_bar = bars + 2 * kStages;
+  uint64_t* tempty_bar = bars + 2 * kStages + 2;
+  uint64_t* drain_bar = bars + 2 * kStages + 4;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  Scheduler sched;
+  sched.init(args, BN, status);
+  if (sched.total == 0 || args.K <= 0) return;  // uniform across the CTA
+  const int Kb = sched.Kb;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull_bar[b], 1);
+      mbar_init(&tempty_bar[b], Cfg::kPromoWarps);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == Cfg::kMmaWarp) {
+    tmem_alloc(tmem_holder, Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == Cfg::kTmaWarp && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  auto fail = [&]() {
+    *abort_flag = 1;
+    raise_status(status, FP8GEMM_ERR_TIMEOUT);
+  };
+
+  if (warp == Cfg::kTmaWarp) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < sched.total && ok; t += gridDim.x) {
+        Tile tile;
+        if (!sched.get(t, BN, tile)) continue;
+        for (int kb = 0; kb < Kb; ++kb, ++it) {
+          const int s = it % kStages;
+          const uint32_t ph = (it / kStages) & 1;
+          if (!mbar_wait(&empty_bar[s], ph ^ 1, abort_flag)) {
+            fail();
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full_bar[s], Cfg::kStageBytes);
+          tma_load_2d(smA + s * Cfg::kABytes, &tmA, &full_bar[s], kb * kBlockK, tile.row0);
+          tma_load_2d(smB + s * Cfg::kBBytes, &tmB, &full_bar[s], kb * kBlockK, tile.b_row0);
+        }
+      }
+      // let the last copies into each stage land before the CTA can exit
+      const uint32_t n = it < uint32_t(kStages) ? it : uint32_t(kStages);
+      for (uint32_t i = it - n; i < it; ++i) drain_wait(&full_bar[i % kStages], (i / kStages) & 1);
+    }
+  } else if (warp == Cfg::kMmaWarp) {
+    // ------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_e4m3_f32(kBlockM, BN);
+      const uint32_t a_base = smem_addr(smA);
+      const uint32_t b_base = smem_addr(smB);
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < sched.total && ok; t += gridDim.x) {
+        Tile tile;
+        if (!sched.get(t, BN, tile)) continue;
+        for (int kb = 0; kb < Kb; ++kb, ++it) {
+          const int s = it % kStages;
+          const uint32_t ph = (it / kStages) & 1;
+          const int buf = it & 1;
+          const uint32_t tph = (it >> 1) & 1;
+          if (!mbar_wait(&tempty_bar[buf], tph ^ 1, abort_flag) ||
+              !mbar_wait(&full_bar[s], ph, abort_flag)) {
+            fail();
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + buf * BN;
+#pragma unroll
+          for (int k = 0; k < kBlockK / 32; ++k) {
+            const uint64_t ad = smem_desc_sw128_kmajor(a_base + s * Cfg::kABytes + k * 32);
+            const uint64_t bd = smem_desc_sw128_kmajor(b_base + s * Cfg::kBBytes + k * 32);
+            umma_e4m3(d_tmem, ad, bd, idesc, k > 0 ? 1u : 0u);
+          }
+          umma_commit(&empty_bar[s]);     // stage free once these MMAs finish
+          umma_commit(&tfull_bar[buf]);   // partial ready for promotion
+        }
+      }
+      if (it > 0) {  // every issued MMA has finished before TMEM is released
+        umma_commit(drain_bar);
+        drain_wait(drain_bar, 0);
+      }
+    }
+  } else {
+    // ------------------------------------------ promotion + epilogue
+    const int wg = warp / 4;                 // column half
+    const int row = (warp % 4) * 32 + lane;  // TMEM lane = tile row
+    const uint32_t lane_base = uint32_t((warp % 4) * 32) << 16;
+    const int Nb = ceil_div(args.N, kBlockK);
+    uint32_t it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < sched.total && ok; t += gridDim.x) {
+      Tile tile;
+      if (!sched.get(t, BN, tile)) continue;
+      const bool row_ok = row < tile.valid_rows;
+      const int col0 = tile.n0 + wg * Cfg::kColsPerWG;  // first column of this warpgroup
+      const bool cols_ok = col0 < args.N;
+      const float* sa_ptr = args.sA + size_t(tile.row0 + row) * Kb;
+      const float* sb_ptr = args.sB + (size_t(tile.e) * Nb + col0 / kBlockK) * Kb;
+
+      float acc[Cfg::kColsPerWG];
+#pragma unroll
+      for (int j = 0; j < Cfg::kColsPerWG; ++j) acc[j] = 0.f;
+
+      float sa_next = row_ok ? __ldg(sa_ptr) : 0.f;
+      float sb_next = cols_ok ? __ldg(sb_ptr) : 0.f;
+      for (int kb = 0; kb < Kb; ++kb, ++it) {
+        const float sc = sa_next * sb_next;
+        if (kb + 1 < Kb) {
+          sa_next = row_ok ? __ldg(sa_ptr + kb + 1) : 0.f;
+          sb_next = cols_ok ? __ldg(sb_ptr + kb + 1) : 0.f;
+        }
+        const int buf = it & 1;
+        const uint32_t tph = (it >> 1) & 1;
+        if (!mbar_wait(&tfull_bar[buf], tph, abort_flag)) {
+          fail();
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + lane_base + buf * BN + wg * Cfg::kColsPerWG;
+#pragma unroll
+        for (int c = 0; c < Cfg::kColsPerWG / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(taddr + c * 32, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) acc[c * 32 + j] = fmaf(__uint_as_float(r[j]), sc, acc[c * 32 + j]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty_bar[buf]);
+      }
+      if (!ok) break;
+      // epilogue: BF16 (round to nearest even), 16-byte stores
+      if (row_ok) {
+        __nv_bfloat16* drow = args.D + size_t(tile.row0 + row) * args.N + col0;
+#pragma unroll
+        for (int j = 0; j < Cfg::kColsPerWG; j += 8) {
+          if (col0 + j < args.N) {
+            uint4 v;
+            __nv_bfloat162 p0 = __floats2bfloat162_rn(acc[j + 0], acc[j + 1]);
+            __nv_bfloat162 p1 = __floats2bfloat162_rn(acc[j + 2], acc[j + 3]);
+            __nv_bfloat162 p2 = __floats2bfloat162_rn(acc[j + 4], acc[j + 5]);
+            __nv_bfloat162 p3 = __floats2bfloat162_rn(acc[j + 6], acc[j + 7]);
+            v.x = *reinterpret_cast<uint32_t*>(&p0);
+            v.y = *reinterpret_cast<uint32_t*>(&p1);
+            v.z = *reinterpret_cast<uint32_t*>(&p2);
+            v.w = *reinterpret_cast<uint32_t*>(&p3);
+            *reinterpret_cast<uint4*>(drow + j) = v;
+          }
+        }
+      }
+    }
+  }
+
+  __syncthreads();
+  if (warp == Cfg::kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+template <class Cfg>
+cudaError_t run(const LaunchCtx& c, const GemmArgs& a) {
+  CUtensorMap tmA, tmB;
+  const uint64_t a_rows = a.mode == GemmMode::kMasked ? uint64_t(a.E) * a.M : uint64_t(a.M);
+  const uint64_t b_rows = uint64_t(a.E) * a.N;
+  if (!make_tmap_u8_sw128(&tmA, a.A, a_rows, a.K, kBlockM)) return cudaErrorInvalidValue;
+  if (!make_tmap_u8_sw128(&tmB, a.B, b_rows, a.K, Cfg::BN)) return cudaErrorInvalidValue;
+
+  auto kern = gemm_tc_kernel<Cfg>;
+  static bool attr_set = false;  // per process; the attribute is per function
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(Cfg::kSmemBytes));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int num_n = ceil_div(a.N, Cfg::BN);
+  long long tiles;
+  if (a.mode == GemmMode::kMasked)
+    tiles = (long long)a.E * ceil_div(a.M, kBlockM) * num_n;
+  else
+    tiles = (long long)ceil_div(a.M, kBlockM) * num_n;
+  const int grid = int(tiles < c.num_sms ? tiles : c.num_sms);
+  if (grid == 0) return cudaSuccess;
+  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, c.stream>>>(tmA, tmB, a, c.status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc(const LaunchCtx& c, const GemmArgs& a) {
+  const bool wide = (a.N % 256 == 0) || a.N >= 2048;
+  if (wide) return run<TcCfg<256, 4>>(c, a);
+  return run<TcCfg<128, 6>>(c, a);
+}
+
+}  // namespace fp8gemm

@@ -1,0 +1,162 @@
+/*
+ * fp8gemm.h -- C ABI of libfp8gemm.so: FP8 (e4m3) GEMM with fine-grained
+ * (1x128 / 128x128) FP32 scales and BF16 output, for GB300 (sm_103a).
+ *
+ * What is computed.  With A e4m3 [M, K] scaled per 1x128 tile (sA [M, Kb]) and
+ * B e4m3 [N, K] scaled per 128x128 tile (sB [Nb, Kb]), Kb = K/128,
+ * Nb = ceil(N/128):
+ *
+ *   D[m, n] = bf16( sum_kb sA[m, kb] * sB[n/128, kb]
+ *                          * sum_{k in block kb} A[m, k] * B[n, k] )
+ *
+ * -- each 128-wide K block is contracted on the tensor cores, then "promoted":
+ * multiplied by its own scale product and added into an FP32 accumulator
+ * ("lpnh.cn/news/2822121" section 2.3; granularity from "blog.hotdry.top:
+ * DeepGEMM FP8 GEMM fine-grained scaling kernels", sections "fine-grained
+ * scaling core design" and "two-level accumulation").  The scale product
+ * sA*sB is formed in FP32 and must be finite.
+ *
+ * Conventions shared by every call:
+ *  - Every pointer is a DEVICE pointer owned by the caller; the library keeps
+ *    no reference after the call returns.  Matrices are row-major with K
+ *    contiguous (D = A * B^T); scale tensors are row-major FP32.
+ *  - Every call is asynchronous on `stream` (0 = legacy default stream): it
+ *    validates on the host, enqueues, and returns.
+ *  - Host-side validation failures return a negative code and enqueue nothing:
+ *    FP8GEMM_ERR_NULL (a required pointer is NULL), FP8GEMM_ERR_ALIGN (a base
+ *    pointer is not 16-byte aligned), FP8GEMM_ERR_SHAPE (negative size,
+ *    K % 128 != 0, N % 8 != 0, M_pad % 128 != 0, or a size past INT32 index
+ *    range), FP8GEMM_ERR_ARCH (the current device is not compute capability
+ *    10.3), FP8GEMM_ERR_LAUNCH (the CUDA launch itself failed).
+ *  - Zero-sized problems (M = 0, M_pad = 0, E = 0, or N = 0) succeed and do
+ *    nothing.
+ *  - Conditions only the device can see (an m_indices entry >= E, a masked_m
+ *    entry > M_max or < 0, a pipeline wait that exceeded its time limit) do
+ *    not trap: the kernel records FP8GEMM_ERR_DEVICE_STATUS or
+ *    FP8GEMM_ERR_TIMEOUT in a per-device status word, skips the offending
+ *    tile and finishes.  Read it with fp8gemm_get_device_status().
+ *  - Inputs and outputs must not overlap.
+ *  - The dense path for M <= 64 splits K across CTAs and reduces partial sums
+ *    through a per-(device, stream) workspace that the library allocates with
+ *    cudaMalloc on the first such call on that stream (about 10 MB, kept until
+ *    process exit).  That first call must therefore not happen during CUDA
+ *    graph capture.  The reduction order is fixed, so results are
+ *    deterministic.
+ */
+#ifndef FP8GEMM_H
+#define FP8GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* fp8gemm_stream_t; /* same handle as cudaStream_t */
+
+enum fp8gemm_status {
+  FP8GEMM_OK = 0,
+  FP8GEMM_ERR_NULL = -1,
+  FP8GEMM_ERR_ALIGN = -2,
+  FP8GEMM_ERR_SHAPE = -3,
+  FP8GEMM_ERR_ARCH = -4,
+  FP8GEMM_ERR_LAUNCH = -5,
+  FP8GEMM_ERR_DEVICE_STATUS = -6,
+  FP8GEMM_ERR_TIMEOUT = -7
+};
+
+/*
+ * fp8_quant_1x128 -- quantise activations per 1x128 tile (online scaling).
+ *
+ * Rule ("news.rkmt.cn/news/5092" section 5.2; rounding from
+ * "lpnh.cn/news/2822121" section 6.3): for each row m and K block kb,
+ *   amax = max |X[m, 128kb : 128kb+128]|,  s = amax / 448  (FP32, IEEE RN),
+ *   Q[m, k] = e4m3(X[m, k] / s)  (FP32 IEEE division, then round to nearest
+ *   even, saturating at +-448),   sX[m, kb] = s.
+ * A block with amax = 0 stores s = 0 and bytes 0x00.  NaN/Inf inputs are
+ * outside the contract.
+ *
+ *   X   f32 [M, K]  (input)         Q  u8 [M, K]  (output, e4m3 bytes)
+ *   sX  f32 [M, K/128] (output)     K % 128 == 0; all pointers 16-B aligned.
+ */
+int fp8_quant_1x128(const float* X, uint8_t* Q, float* sX, int M, int K,
+                    fp8gemm_stream_t stream);
+
+/*
+ * fp8_quant_128x128 -- quantise weights per 128x128 tile (the offline step
+ * that prepares B; same rule, amax over the whole tile; ragged last row tile
+ * allowed).  Batched over E independent matrices (E = 1 for a dense B).
+ *
+ *   W   f32 [E, N, K] (input)       Q  u8 [E, N, K] (output)
+ *   sW  f32 [E, ceil(N/128), K/128] (output)
+ */
+int fp8_quant_128x128(const float* W, uint8_t* Q, float* sW, int E, int N, int K,
+                      fp8gemm_stream_t stream);
+
+/*
+ * fp8gemm_dense -- D = A * B^T with block scales ("lpnh.cn/news/2822121"
+ * section 4.1 dense main loop; scaling as above).
+ *
+ *   A  u8 [M, K]   sA f32 [M, K/128]
+ *   B  u8 [N, K]   sB f32 [ceil(N/128), K/128]
+ *   D  bf16 [M, N] (output, written in full)
+ *   M >= 0, N % 8 == 0, K % 128 == 0, K > 0.
+ */
+int fp8gemm_dense(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                  void* D, int M, int N, int K, fp8gemm_stream_t stream);
+
+/*
+ * fp8gemm_grouped_contiguous -- MoE experts in one launch, each expert's
+ * tokens a contiguous row segment of A ("news.rkmt.cn/news/5092" section 5.3;
+ * "news.rkmt.cn/news/5092" section 1.2: one launch for many experts).
+ *
+ *   A  u8 [M_pad, K]          sA f32 [M_pad, K/128]
+ *   B  u8 [E, N, K]           sB f32 [E, ceil(N/128), K/128]
+ *   m_indices i32 [M_pad] (device): expert of each row, -1 for padding rows
+ *   D  bf16 [M_pad, N] (output; padding rows are left unspecified)
+ *   M_pad % 128 == 0, and every 128-row block holds rows of a single expert
+ *   (segments padded to 128 rows, padding at each segment's end).  Only the
+ *   first row's index of each block is read; a block whose first index is -1
+ *   is skipped; an index >= E sets FP8GEMM_ERR_DEVICE_STATUS.
+ */
+int fp8gemm_grouped_contiguous(const uint8_t* A, const float* sA, const uint8_t* B,
+                               const float* sB, const int32_t* m_indices, void* D,
+                               int M_pad, int N, int K, int E, fp8gemm_stream_t stream);
+
+/*
+ * fp8gemm_grouped_masked -- MoE experts with per-expert valid-row counts kept
+ * in device memory, so the launch shape is fixed and a CUDA graph can be
+ * replayed with new counts ("bhfrc.com/news/60211" section 4.3; skipping
+ * empty blocks, "lpnh.cn/news/2822121" section 5.2).
+ *
+ *   A  u8 [E, M_max, K]       sA f32 [E, M_max, K/128]
+ *   B  u8 [E, N, K]           sB f32 [E, ceil(N/128), K/128]
+ *   masked_m i32 [E] (device): rows of expert e to compute, 0..M_max
+ *   D  bf16 [E, M_max, N] (output: rows >= masked_m[e] are NOT written)
+ *   A masked_m entry outside [0, M_max] is clamped and sets
+ *   FP8GEMM_ERR_DEVICE_STATUS.
+ */
+int fp8gemm_grouped_masked(const uint8_t* A, const float* sA, const uint8_t* B,
+                           const float* sB, const int32_t* masked_m, void* D,
+                           int E, int M_max, int N, int K, fp8gemm_stream_t stream);
+
+/*
+ * fp8gemm_get_device_status -- synchronise `stream`, then read and clear the
+ * current device's status word: *out = FP8GEMM_OK, FP8GEMM_ERR_DEVICE_STATUS
+ * or FP8GEMM_ERR_TIMEOUT.  Returns FP8GEMM_OK, or FP8GEMM_ERR_NULL /
+ * FP8GEMM_ERR_LAUNCH if `out` is NULL or the CUDA calls fail.
+ */
+int fp8gemm_get_device_status(fp8gemm_stream_t stream, int* out);
+
+/* fp8gemm_strerror -- static description of a status code. */
+const char* fp8gemm_strerror(int code);
+
+/* fp8gemm_num_kernel_launches -- kernels this process enqueued through the
+ * library so far (all devices); a host-side counter for launch accounting. */
+uint64_t fp8gemm_num_kernel_launches(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8GEMM_H */

@@ -1,0 +1,72 @@
+"""The C-ABI library builds, loads and exports every declared entry point;
+host-side validation answers without touching a GPU.  CPU only."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?[\w\s\*]+?\b(\w+)\s*\([^;{]*\)\s*;", src, re.M)
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from fp8_fine_grained_e4m3_gb300 import build, binding
+    build.build()
+    return binding.lib()
+
+
+def test_header_declares_the_boundary():
+    names = set(_declared_functions())
+    for n in ["fp8_quant_1x128", "fp8_quant_128x128", "fp8gemm_dense",
+              "fp8gemm_grouped_contiguous", "fp8gemm_grouped_masked",
+              "fp8gemm_get_device_status", "fp8gemm_strerror"]:
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in _declared_functions():
+        assert hasattr(lib, n), n
+
+
+def test_binding_covers_every_symbol():
+    from fp8_fine_grained_e4m3_gb300 import binding
+    bound = {n for n, _, _ in binding.SIGNATURES}
+    assert set(_declared_functions()) <= bound
+
+
+def test_strerror_on_host(lib):
+    from fp8_fine_grained_e4m3_gb300 import binding
+    assert binding.strerror(binding.ERR_SHAPE).startswith("unsupported shape")
+    assert binding.strerror(12345) == "unknown status"
+
+
+def test_host_validation_needs_no_gpu(lib):
+    from fp8_fine_grained_e4m3_gb300 import binding as b
+    P = ctypes.c_void_p
+    good = P(1 << 20)  # never dereferenced: validation fails before any CUDA call
+    s = P(0)
+    assert lib.fp8gemm_dense(good, good, good, good, good, 128, 256, 200, s) == b.ERR_SHAPE
+    assert lib.fp8gemm_dense(good, good, good, good, good, 128, 250, 256, s) == b.ERR_SHAPE
+    assert lib.fp8gemm_dense(None, good, good, good, good, 128, 256, 256, s) == b.ERR_NULL
+    assert lib.fp8gemm_dense(P((1 << 20) + 4), good, good, good, good, 128, 256, 256, s) == b.ERR_ALIGN
+    assert lib.fp8gemm_dense(good, good, good, good, good, 0, 256, 256, s) == b.OK
+    assert lib.fp8gemm_grouped_contiguous(good, good, good, good, good, good,
+                                          100, 256, 256, 2, s) == b.ERR_SHAPE
+    assert lib.fp8gemm_grouped_masked(good, good, good, good, good, good,
+                                      0, 128, 256, 256, s) == b.OK
+    assert lib.fp8_quant_1x128(good, good, good, 4, 130, s) == b.ERR_SHAPE
+    assert lib.fp8_quant_128x128(good, None, good, 1, 8, 128, s) == b.ERR_NULL
+    assert lib.fp8gemm_get_device_status(s, None) == b.ERR_NULL
+    assert isinstance(lib.fp8gemm_num_kernel_launches(), int)

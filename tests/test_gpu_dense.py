@@ -1,0 +1,79 @@
+"""Dense GEMM on the GPU vs the FP64 oracle (per-element acceptance test)."""
+
+import numpy as np
+import pytest
+
+from tests.gpu_helpers import (assert_close, dev, host, ogemm, quantised_dense,
+                               sample_rows_cols)
+
+pytestmark = pytest.mark.gpu
+
+
+def _b():
+    from fp8_fine_grained_e4m3_gb300 import binding
+    return binding
+
+
+def _run(A, sA, B, sB):
+    return host(_b().fp8gemm_dense(dev(A), dev(sA), dev(B), dev(sB)))
+
+
+@pytest.mark.parametrize("M,N,K,kind", [
+    (128, 256, 512, "normal"),      # the correctness configuration, whole
+    (300, 520, 1024, "normal"),     # ragged M and N, several tiles (128-wide N tiles)
+    (256, 512, 640, "prefill"),     # 256-wide N tiles, outlier columns
+    (65, 256, 256, "normal"),       # smallest M on the large-M path
+    (520, 2304, 384, "prefill"),    # many tiles, 256-wide N tiles, ragged M
+    (1, 7168, 2048, "decode"),      # decode shapes, whole
+    (16, 7168, 2048, "decode"),
+    (64, 7168, 2048, "decode"),
+    (1, 2048, 7168, "decode"),
+    (16, 2048, 7168, "decode"),
+    (64, 2048, 7168, "decode"),
+    (5, 264, 384, "normal"),        # small M, ragged N tile
+    (33, 1000, 1280, "normal"),
+    (17, 128, 16384, "decode"),     # split-K over one N tile
+])
+def test_dense_matches_oracle(M, N, K, kind):
+    A, sA, B, sB = quantised_dense(M, N, K, kind, seed=M * 7 + N)
+    got = _run(A, sA, B, sB)
+    ref = ogemm.gemm_dense(A, sA, B, sB)
+    assert_close(got, ref, f"dense {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M", [1, 16, 64])
+def test_small_m_is_deterministic(M):
+    A, sA, B, sB = quantised_dense(M, 7168, 2048, "decode", seed=3)
+    b = _b()
+    tA, tsA, tB, tsB = dev(A), dev(sA), dev(B), dev(sB)
+    d1 = host(b.fp8gemm_dense(tA, tsA, tB, tsB))
+    d2 = host(b.fp8gemm_dense(tA, tsA, tB, tsB))
+    assert np.array_equal(d1, d2)
+
+
+def test_extreme_scales():
+    """Large and tiny block scales whose products stay finite in FP32; errors
+    must not concentrate in any K block."""
+    M, N, K = 130, 256, 1024
+    A, sA, B, sB = quantised_dense(M, N, K, "normal", seed=11)
+    g = np.random.default_rng(12)
+    sA = (sA * (2.0 ** g.integers(-60, 60, sA.shape))).astype(np.float32)
+    sB = (sB * (2.0 ** g.integers(-40, 40, sB.shape))).astype(np.float32)
+    got = _run(A, sA, B, sB)
+    ref = ogemm.gemm_dense(A, sA, B, sB)
+    assert_close(got, ref, "extreme scales")
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("M,N,K", [(4096, 4096, 4096), (4096, 7168, 16384)])
+def test_prefill_full_size_sampled(M, N, K):
+    """Full prefill size, launched exactly as the benchmark does; the oracle
+    computes a sample of rows x columns (including the last tile's edges)."""
+    A, sA, B, sB = quantised_dense(M, N, K, "prefill", seed=0)
+    got = _run(A, sA, B, sB)
+    rows, cols = sample_rows_cols(M, N, 48, 96, seed=1)
+    rows = np.unique(np.concatenate([rows, [127, 128, M - 128]]))
+    cols = np.unique(np.concatenate([cols, [255, 256, N - 256]]))
+    ref = ogemm.gemm_dense_at(A, sA, B, sB, rows, cols)
+    assert_close(got[rows][:, cols], ref, f"prefill {M}x{N}x{K}")
+    assert np.isfinite(got).all()

@@ -142,3 +142,11 @@ def test_grouped_weight_quant_is_per_expert():
     for e in range(3):
         q, s = quant.quant_128x128(W[e])
         assert np.array_equal(Q[e], q) and np.array_equal(S[e], s)
+
+
+def test_quant_128x128_fast_equals_loop():
+    _, W = synthetic.dense_operands(8, 300, 512, kind="decode", seed=10)
+    W[128:256, 128:256] = 0.0  # an all-zero tile
+    Q1, S1 = quant.quant_128x128(W)
+    Q2, S2 = quant.quant_128x128_fast(W)
+    assert np.array_equal(Q1, Q2) and np.array_equal(S1, S2)
