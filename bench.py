@@ -1,0 +1,619 @@
+#!/usr/bin/env python
+"""Benchmark of the FP8 block-scaled GEMM hot path on GB300.
+
+One step = the whole hot path over one batch of the dense prefill workload:
+for each of the two prefill shapes (M, N, K) = (4096, 7168, 16384) and
+(4096, 4096, 4096): quantise the FP32 activations per 1x128 tile
+(fp8_quant_1x128) and run the block-scaled GEMM (fp8gemm_dense) against
+weights quantised per 128x128 tile beforehand (the offline step, untimed).
+Inputs are synthetic (A ~ N(0,1) with 1 % outlier columns x50, B ~ N(0,0.02)),
+drawn and kept on the device; L2 is flushed (a 256 MB write) before every
+timed step; each step is timed with CUDA events on the launching stream.
+
+Printed: one JSON line (rank 0).  `value` is TFLOP/s over all ranks;
+`roofline` describes the GEMM kernel; `e2e` repeats the step through the
+public API with host (pinned) inputs and outputs, copies included;
+`cpu_baseline` times the CPU oracle on a bounded sample; `configs` adds
+measurements of the other workloads (correctness case, decode shapes, MoE
+contiguous and masked, the quantiser) against their own rooflines.
+
+`--impl reference` times the CPU oracle as the reference arm instead.
+Multi-GPU (torchrun): every rank runs the same workload on its own GPU
+(replicas; no collective on the data path).
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+PREFILL_SHAPES = [(4096, 7168, 16384), (4096, 4096, 4096)]
+METRIC = "FP8 block-scaled GEMM TFLOPS & GB/s, % of GB300 roofline (dense/grouped)"
+UNIT = "TFLOP/s"
+WORKLOAD = ("dense prefill FP8 e4m3 GEMM, 1x128 A / 128x128 B FP32 scales, BF16 out: "
+            "quantise A + GEMM for (M,N,K) = (4096,7168,16384) and (4096,4096,4096)")
+FLUSH_BYTES = 256 << 20
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16": p["bf16_tflops"],
+                "bf16_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+
+
+def fp8_peak(peaks, sustained=True):
+    # FP8 dense tensor rate = 2 x BF16 (nominal 4.5 vs 2.25 PFLOP/s)
+    return 2.0 * (peaks["bf16_sustained"] if sustained else peaks["bf16"])
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.strip().split(", ") for r in self.file.read().splitlines() if r.strip()]
+        self.file.close()
+        os.unlink(self.file.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except (ValueError, IndexError):
+                continue
+            for name, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------- GPU arm
+def gemm_bytes(M, N, K, e_active=1, rows=None):
+    """Algorithmic bytes of one block-scaled GEMM: A and its scales for the
+    real rows, B and its scales for the active experts, D for the real rows."""
+    rows = M if rows is None else rows
+    Kb = K // 128
+    Nb = -(-N // 128)
+    return rows * K + 4 * rows * Kb + e_active * (N * K + 4 * Nb * Kb) + 2 * rows * N
+
+
+def run_gpu(args, rank, world):
+    import torch
+
+    from fp8_fine_grained_e4m3_gb300 import binding as b
+    from fp8_fine_grained_e4m3_gb300 import synthetic
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+    dev = torch.device("cuda", torch.cuda.current_device())
+    peaks = load_peaks()
+    stream = torch.cuda.current_stream()
+
+    # ---- inputs resident in HBM; weights quantised once (offline step)
+    cases = []
+    for i, (M, N, K) in enumerate(PREFILL_SHAPES):
+        X, W = synthetic.dense_operands_device(M, N, K, kind="prefill", seed=i, device=dev)
+        B8, sB = b.fp8_quant_128x128(W)
+        del W
+        A8 = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        sA = torch.empty((M, K // 128), dtype=torch.float32, device=dev)
+        D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        cases.append(dict(M=M, N=N, K=K, X=X, A8=A8, sA=sA, B8=B8, sB=sB, D=D))
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flops_step = sum(2.0 * c["M"] * c["N"] * c["K"] for c in cases)
+
+    def step(gemm_events=None):
+        # both quantisers first: while they run, the host enqueues the GEMMs,
+        # so the device never waits on the host inside a step
+        for c in cases:
+            b.fp8_quant_1x128(c["X"], Q=c["A8"], sX=c["sA"])
+        for j, c in enumerate(cases):
+            if gemm_events is not None:
+                gemm_events[j][0].record(stream)
+            b.fp8gemm_dense(c["A8"], c["sA"], c["B8"], c["sB"], D=c["D"])
+            if gemm_events is not None:
+                gemm_events[j][1].record(stream)
+
+    for i in range(args.warmup):
+        flush.fill_(i & 0xFF)
+        step()
+    torch.cuda.synchronize()
+    if b.fp8gemm_get_device_status() != b.OK:
+        raise RuntimeError("device status set during warm-up")
+
+    K_steps = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K_steps)]
+    gev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in cases] for _ in range(K_steps)]
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    launches0 = b.num_kernel_launches()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    for i in range(K_steps):
+        flush.fill_(i & 0xFF)  # L2 flush, outside the timed interval
+        ev[i][0].record(stream)
+        step(gev[i])
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    launches = b.num_kernel_launches() - launches0
+    clk = clocks.stop()
+    status = b.fp8gemm_get_device_status()
+    if status != b.OK:
+        raise RuntimeError(f"device status {status} after the timed region")
+
+    step_ms = [s.elapsed_time(e) for s, e in ev]
+    ms_per_step = sum(step_ms) / K_steps
+    gemm_ms = [sum(g[j][0].elapsed_time(g[j][1]) for g in gev) / K_steps
+               for j in range(len(cases))]
+    if world > 1:
+        t = torch.tensor([ms_per_step], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_per_step = float(t.item())
+    value = world * flops_step / (ms_per_step * 1e-3) / 1e12
+
+    # roofline of the dominant kernel: the dense GEMM on the 4096x7168x16384
+    # shape (about 80 % of the step); the other shape is listed beside it
+    gemm_flops = [2.0 * c["M"] * c["N"] * c["K"] for c in cases]
+    achieved = gemm_flops[0] / (gemm_ms[0] * 1e-3) / 1e12
+    peak = fp8_peak(peaks, sustained=True)
+    roofline = {"kernel": "gemm_tc_kernel<BN=256> (fp8gemm_dense, M > 64), M=4096 N=7168 K=16384",
+                "bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1),
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                "peak_source": (f"{peaks['source']} bf16 sustained x 2 (FP8/BF16 nominal "
+                                "ratio); the kernel runs back to back for seconds"),
+                "frac_of_burst_peak": round(achieved / fp8_peak(peaks, False), 4),
+                "traffic": traffic_from_profiles("gemm_tc_dense_4096x7168x16384"),
+                "algorithmic_bytes": gemm_bytes(*PREFILL_SHAPES[0]),
+                "per_shape": [{"M": c["M"], "N": c["N"], "K": c["K"],
+                               "gemm_us": round(1e3 * t, 2),
+                               "tflops": round(f / (t * 1e-3) / 1e12, 1)}
+                              for c, t, f in zip(cases, gemm_ms, gemm_flops)]}
+
+    # ---- end to end through the public API with host buffers
+    e2e = measure_e2e(args, cases, flops_step, world)
+
+    out = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+           "steps": K_steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": "e4m3 (FP8 products, FP32 accumulate, BF16 out)", "data": "synthetic",
+           "config": {"workload": WORKLOAD,
+                      "l2": "flushed before every timed step (256 MB device write)",
+                      "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                      "timing": "CUDA events per step on the launching stream"},
+           "roofline": roofline, "e2e": e2e, "gpu_launches": int(launches),
+           "clocks": clk, "impl": "gb300"}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_seconds)
+    if rank == 0 and not args.no_extras:
+        for c in cases:
+            del c["X"]
+        del cases
+        torch.cuda.empty_cache()
+        out["configs"] = measure_configs(peaks, dev)
+    return out
+
+
+def measure_e2e(args, cases, flops_step, world):
+    """The step through the public API with pinned host input and output:
+    H2D copy of X, quantise, GEMM, D2H copy of D -- all inside the timed
+    interval (CUDA events around the whole sequence)."""
+    import torch
+
+    from fp8_fine_grained_e4m3_gb300 import binding as b
+    stream = torch.cuda.current_stream()
+    hosts = []
+    h2d = d2h = 0
+    for c in cases:
+        Xh = torch.empty(c["X"].shape, dtype=torch.float32, pin_memory=True)
+        Xh.copy_(c["X"])
+        Dh = torch.empty(c["D"].shape, dtype=torch.bfloat16, pin_memory=True)
+        hosts.append((Xh, Dh))
+        h2d += Xh.numel() * 4
+        d2h += Dh.numel() * 2
+    n = max(3, min(args.steps, 20))
+    times = []
+    for i in range(n + 2):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for c, (Xh, Dh) in zip(cases, hosts):
+            c["X"].copy_(Xh, non_blocking=True)
+            b.fp8_quant_1x128(c["X"], Q=c["A8"], sX=c["sA"])
+            b.fp8gemm_dense(c["A8"], c["sA"], c["B8"], c["sB"], D=c["D"])
+            Dh.copy_(c["D"], non_blocking=True)
+        e.record(stream)
+        e.synchronize()
+        if i >= 2:
+            times.append(s.elapsed_time(e))
+    ms = sum(times) / len(times)
+    return {"value": round(world * flops_step / (ms * 1e-3) / 1e12, 2), "unit": UNIT,
+            "ms_per_step": round(ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": n}
+
+
+def time_launch(fn, flush, n=20, warm=3):
+    """Mean device time (ms) of fn() over n launches, L2 flushed before each."""
+    import torch
+    stream = torch.cuda.current_stream()
+    for i in range(warm):
+        fn()
+    ts = []
+    for i in range(n):
+        flush.fill_(i & 0xFF)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        fn()
+        e.record(stream)
+        ts.append((s, e))
+    torch.cuda.synchronize()
+    return sum(s.elapsed_time(e) for s, e in ts) / n
+
+
+def time_graph(fns, reps=4):
+    """Mean device time (ms) per call of the closures in `fns`, captured once
+    each into a CUDA graph (in order) and replayed `reps` times."""
+    import torch
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):  # first calls (workspace, attributes) before capture
+        for fn in fns:
+            fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for fn in fns:
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    st, en = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    st.record()
+    for _ in range(reps):
+        g.replay()
+    en.record()
+    torch.cuda.synchronize()
+    return st.elapsed_time(en) / (reps * len(fns))
+
+
+def _roof(flops, nbytes, ms, peaks, sustained=False):
+    t_c = flops / (fp8_peak(peaks, sustained) * 1e12)
+    t_m = nbytes / (peaks["hbm_gbs"] * 1e9)
+    t = ms * 1e-3
+    return {"us": round(ms * 1e3, 2), "tflops": round(flops / t / 1e12, 1),
+            "gbs": round(nbytes / t / 1e9, 1), "bound": "tensor" if t_c > t_m else "hbm",
+            "roofline_frac": round(max(t_c, t_m) / t, 4)}
+
+
+def measure_configs(peaks, dev):
+    """The other workloads, each timed alone (L2 flushed) against its own
+    roofline max(FLOP / FP8 peak, bytes / HBM peak), burst peaks."""
+    import numpy as np
+    import torch
+
+    from fp8_fine_grained_e4m3_gb300 import binding as b
+    from fp8_fine_grained_e4m3_gb300 import synthetic
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    res = {}
+
+    def dense_case(M, N, K, kind, seed):
+        X, W = synthetic.dense_operands_device(M, N, K, kind=kind, seed=seed, device=dev)
+        A8, sA = b.fp8_quant_1x128(X)
+        B8, sB = b.fp8_quant_128x128(W)
+        del X, W
+        D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        return A8, sA, B8, sB, D
+
+    A8, sA, B8, sB, D = dense_case(128, 256, 512, "normal", 0)
+    ms = time_launch(lambda: b.fp8gemm_dense(A8, sA, B8, sB, D=D), flush)
+    res["dense_128x256x512"] = _roof(2 * 128 * 256 * 512, gemm_bytes(128, 256, 512), ms, peaks)
+
+    for M in (1, 16, 64):
+        for (N, K) in ((7168, 2048), (2048, 7168)):
+            # 24 weight copies (> 2x L2 in total) used in turn, launched back to
+            # back from a CUDA graph, so each launch reads its weights from HBM
+            # and no host launch overhead sits between launches
+            A8, sA, B8, sB, D = dense_case(M, N, K, "decode", M)
+            copies = [(B8.clone(), sB.clone()) for _ in range(24)]
+            fns = [(lambda Bc=Bc, sBc=sBc: b.fp8gemm_dense(A8, sA, Bc, sBc, D=D))
+                   for Bc, sBc in copies]
+            ms = time_graph(fns, reps=4)
+            r = _roof(2 * M * N * K, gemm_bytes(M, N, K), ms, peaks)
+            r["timing"] = "CUDA graph, 24 rotating weight copies"
+            res[f"decode_{M}x{N}x{K}"] = r
+            del copies, fns
+
+    # quantiser on the large prefill activations
+    X, _ = synthetic.dense_operands_device(4096, 8, 16384, kind="prefill", seed=0, device=dev)
+    Q = torch.empty(X.shape, dtype=torch.uint8, device=dev)
+    S = torch.empty((4096, 128), dtype=torch.float32, device=dev)
+    ms = time_launch(lambda: b.fp8_quant_1x128(X, Q=Q, sX=S), flush)
+    nb = X.numel() * 5 + S.numel() * 4
+    res["quant_1x128_4096x16384"] = {"us": round(ms * 1e3, 2),
+                                     "gbs": round(nb / (ms * 1e-3) / 1e9, 1),
+                                     "bound": "hbm",
+                                     "roofline_frac": round(nb / (peaks["hbm_gbs"] * 1e9) /
+                                                            (ms * 1e-3), 4)}
+    del X, Q, S
+
+    # MoE contiguous: 32 experts, 8192 Zipf(1.1) tokens, N=4096, K=7168
+    E, T, N, K = 32, 8192, 4096, 7168
+    lay = synthetic.contiguous_layout(synthetic.zipf_counts(E, T, seed=0))
+    X = synthetic.contiguous_activations_device(lay, K, seed=0, device=dev)
+    A8, sA = b.fp8_quant_1x128(X)
+    del X
+    W = synthetic.expert_weights_device(E, N, K, seed=0, device=dev)
+    B8, sB = b.fp8_quant_128x128(W)
+    del W
+    mi = torch.from_numpy(lay.m_indices).to(dev)
+    D = torch.empty((lay.M_pad, N), dtype=torch.bfloat16, device=dev)
+    ms = time_launch(lambda: b.fp8gemm_grouped_contiguous(A8, sA, B8, sB, mi, D=D), flush)
+    rows = int(lay.counts.sum())
+    e_act = int((lay.counts > 0).sum())
+    nbytes = gemm_bytes(rows, N, K, e_active=e_act, rows=rows) + 4 * lay.M_pad
+    r = _roof(2.0 * rows * N * K, nbytes, ms, peaks)
+    r["note"] = "padding rows not credited"
+    res["moe_contiguous_E32_T8192_N4096_K7168"] = r
+    del A8, sA, B8, sB, D
+    torch.cuda.empty_cache()
+
+    # MoE masked: 16 experts, A [16, 256, 7168] Student-t, masked_m ~ U[0, 256]
+    E, M_max, N, K = 16, 256, 4096, 7168
+    mm = synthetic.masked_counts(E, M_max, seed=0)
+    X = synthetic.masked_activations_device(E, M_max, K, seed=0, device=dev)
+    A8, sA = b.fp8_quant_1x128(X)
+    del X
+    W = synthetic.expert_weights_device(E, N, K, seed=1, device=dev)
+    B8, sB = b.fp8_quant_128x128(W)
+    del W
+    mmd = torch.from_numpy(mm).to(dev)
+    D = torch.empty((E, M_max, N), dtype=torch.bfloat16, device=dev)
+    ms = time_launch(lambda: b.fp8gemm_grouped_masked(A8, sA, B8, sB, mmd, D=D), flush)
+    rows = int(mm.sum())
+    e_act = int((mm > 0).sum())
+    nbytes = gemm_bytes(rows, N, K, e_active=e_act, rows=rows) + 4 * E
+    r = _roof(2.0 * rows * N * K, nbytes, ms, peaks)
+    r["note"] = f"sum(masked_m) = {rows}; masked-out rows not credited"
+    res["moe_masked_E16_M256_N4096_K7168"] = r
+    del A8, sA, B8, sB, D
+    torch.cuda.empty_cache()
+    if b.fp8gemm_get_device_status() != b.OK:
+        raise RuntimeError("device status set while measuring the other workloads")
+    return res
+
+
+KERNEL_SOURCES = ["gemm_tc.cu", "ptx.cuh", "common.cuh"]
+
+
+def kernel_source_hash(files=KERNEL_SOURCES):
+    import hashlib
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "fp8_fine_grained_e4m3_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profiles(key):
+    """DRAM bytes (read + write) per launch from the committed ncu summary
+    profiles/traffic.json -- only if it was taken on the current kernel
+    source (same hash); None otherwise."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        t = json.load(f).get(key)
+    if not t or t.get("source_hash") != kernel_source_hash(t.get("sources", KERNEL_SOURCES)):
+        return None
+    return t["dram_bytes_per_launch"]
+
+
+# ------------------------------------------------------------ CPU oracle
+def _oracle_sample(rows, cols, seed=0):
+    """Inputs for the oracle timing: the prefill shapes restricted to `rows`
+    rows of A and `cols` rows of B (whole 128-row scale tiles), same K and
+    same value recipe; B is quantised here (untimed, like the offline step)."""
+    import numpy as np
+
+    from fp8_fine_grained_e4m3_gb300 import synthetic
+    from oracle import quant as oq
+    out = []
+    for i, (M, N, K) in enumerate(PREFILL_SHAPES):
+        X, W = synthetic.dense_operands(rows, cols, K, kind="prefill", seed=seed + i)
+        Bq, sB = oq.quant_128x128_fast(W)
+        out.append((X, Bq, sB, K))
+    return out
+
+
+def _oracle_step(sample):
+    from oracle import gemm as og
+    from oracle import quant as oq
+    flops = 0.0
+    for X, Bq, sB, K in sample:
+        A, sA = oq.quant_1x128(X)
+        og.gemm_dense(A, sA, Bq, sB)
+        flops += 2.0 * X.shape[0] * Bq.shape[0] * K
+    return flops
+
+
+def cpu_baseline(budget_s=15.0):
+    """The oracle (quantise A rows + FP64 block-scaled GEMM), as it stands,
+    on a sample of the step: 16 rows of A x 1024 rows of B per prefill shape,
+    repeated for about `budget_s` seconds of host time."""
+    sample = _oracle_sample(16, 1024)
+    t0 = time.perf_counter()
+    flops = 0.0
+    reps = 0
+    while True:
+        flops += _oracle_step(sample)
+        reps += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": (f"{reps} x [16 rows of A x 1024 rows of B, full K] per prefill shape "
+                       f"(quantise A rows + FP64 block-scaled GEMM), {dt:.1f} s")}
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the CPU oracle timed on the host cores, one bounded
+    sample (4 rows of A x 128 rows of B per prefill shape) per step."""
+    if rank != 0:
+        return None
+    sample = _oracle_sample(4, 128, seed=1)
+    for _ in range(args.warmup):
+        _oracle_step(sample)
+    t0 = time.perf_counter()
+    flops = 0.0
+    for _ in range(args.steps):
+        flops += _oracle_step(sample)
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * dt / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": WORKLOAD, "sample": "4 rows of A x 128 rows of B per shape"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(),
+                             "kind": "oracle",
+                             "sample": "4 rows of A x 128 rows of B, full K, per prefill shape"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def run_kernel_case(name, reps):
+    """Launch one kernel of the path `reps` times on a fixed case, nothing
+    else timed or printed: the target of the ncu captures."""
+    import torch
+
+    from fp8_fine_grained_e4m3_gb300 import binding as b
+    from fp8_fine_grained_e4m3_gb300 import synthetic
+    dev = torch.device("cuda", 0)
+    shapes = {"gemm_prefill": (4096, 7168, 16384), "gemm_square": (4096, 4096, 4096),
+              "gemm_decode64": (64, 7168, 2048), "gemm_decode1": (1, 7168, 2048),
+              "quant": (4096, 8, 16384)}
+    if name in shapes:
+        M, N, K = shapes[name]
+        X, W = synthetic.dense_operands_device(M, N, K, kind="prefill", seed=0, device=dev)
+        A8, sA = b.fp8_quant_1x128(X)
+        B8, sB = b.fp8_quant_128x128(W)
+        D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        if name == "quant":
+            fn = lambda: b.fp8_quant_1x128(X, Q=A8, sX=sA)  # noqa: E731
+        else:
+            del X, W
+            fn = lambda: b.fp8gemm_dense(A8, sA, B8, sB, D=D)  # noqa: E731
+    elif name in ("contiguous", "masked"):
+        if name == "contiguous":
+            E, N, K = 32, 4096, 7168
+            lay = synthetic.contiguous_layout(synthetic.zipf_counts(E, 8192, seed=0))
+            X = synthetic.contiguous_activations_device(lay, K, seed=0, device=dev)
+            info = torch.from_numpy(lay.m_indices).to(dev)
+            D = torch.empty((lay.M_pad, N), dtype=torch.bfloat16, device=dev)
+        else:
+            E, N, K = 16, 4096, 7168
+            X = synthetic.masked_activations_device(E, 256, K, seed=0, device=dev)
+            info = torch.from_numpy(synthetic.masked_counts(E, 256, seed=0)).to(dev)
+            D = torch.empty((E, 256, N), dtype=torch.bfloat16, device=dev)
+        A8, sA = b.fp8_quant_1x128(X)
+        del X
+        B8, sB = b.fp8_quant_128x128(synthetic.expert_weights_device(E, N, K, device=dev))
+        if name == "contiguous":
+            fn = lambda: b.fp8gemm_grouped_contiguous(A8, sA, B8, sB, info, D=D)  # noqa: E731
+        else:
+            fn = lambda: b.fp8gemm_grouped_masked(A8, sA, B8, sB, info, D=D)  # noqa: E731
+    else:
+        raise SystemExit(f"unknown kernel case {name}")
+    torch.cuda.synchronize()
+    for _ in range(reps):
+        fn()
+    torch.cuda.synchronize()
+    st = b.fp8gemm_get_device_status()
+    print(json.dumps({"kernel_case": name, "reps": reps, "status": st}))
+    if st != b.OK:
+        raise SystemExit(1)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--kernel-case", default=None,
+                    help="launch one kernel case --reps times (profiling target) and exit")
+    ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--no-extras", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    if args.kernel_case:
+        run_kernel_case(args.kernel_case, args.reps)
+        return
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        torch.distributed.init_process_group("nccl")
+    out = run_gpu(args, rank, world)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

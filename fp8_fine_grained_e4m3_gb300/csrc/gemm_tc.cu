@@ -12,13 +12,16 @@
 // level promoted to FP32 on the CUDA cores).  The result is rounded to BF16
 // once, in the epilogue.
 //
-// CTA layout (320 threads, one CTA per SM, persistent over tiles):
+// CTA layout (384 threads, one CTA per SM, persistent over tiles):
 //   warps 0-7  promotion + epilogue: two warpgroups; warpgroup g owns columns
 //              [g*BN/2, (g+1)*BN/2) of the tile, thread = tile row (TMEM lane)
 //   warp 8     TMA producer: A tile 128x128 B and B tile BNx128 B per K block
 //              into a kStages-deep shared-memory ring (128-byte swizzle)
 //   warp 9     MMA issuer (one thread): 4 x tcgen05.mma kind::f8f6f4 (K = 32)
 //              per K block into one of two TMEM partial buffers
+//   warps 10-11 idle: they complete the third warpgroup, whose register
+//              budget is lowered (setmaxnreg) so the promotion warpgroups can
+//              hold a 128-column FP32 accumulator per thread
 // Synchronisation is by mbarriers only: full/empty per ring stage, and
 // tmem_full/tmem_empty per TMEM buffer, so the tensor cores work on K block
 // kb+1 while the promotion warps drain K block kb.  ("lpnh.cn/news/2822121"
@@ -46,7 +49,12 @@ struct TcCfg {
   static constexpr int kPromoWarps = 8;
   static constexpr int kTmaWarp = 8;
   static constexpr int kMmaWarp = 9;
-  static constexpr int kThreads = 320;
+  static constexpr int kThreads = 384;  // 3 warpgroups; warps 10-11 only donate registers
+  // Launch cap is 65536 / 384 -> 168 registers.  The producer warpgroup drops
+  // to kLowRegs and the two promotion warpgroups rise to kHighRegs:
+  // 4*32*104 + 8*32*200 = 64512 = 384*168.
+  static constexpr uint32_t kLowRegs = 104;
+  static constexpr uint32_t kHighRegs = 200;
   static constexpr int kABytes = kBlockM * kBlockK;  // 16 KB
   static constexpr int kBBytes = BN * kBlockK;
   static constexpr int kStageBytes = kABytes + kBBytes;
@@ -68,9 +76,11 @@ struct Tile {
 
 // Walks the same tile sequence in every role of every CTA.
 struct Scheduler {
-  GemmArgs a;
+  const GemmArgs& a;  // the kernel parameter itself (param space), not a copy
   int num_m, num_n, Kb, total;
   int* status;
+
+  __device__ Scheduler(const GemmArgs& args, int BN, int* st) : a(args) { init(BN, st); }
 
   __device__ int masked_rows(int e) const {
     int m = __ldg(a.group_info + e);
@@ -81,8 +91,7 @@ struct Scheduler {
     return m;
   }
 
-  __device__ void init(const GemmArgs& args, int BN, int* st) {
-    a = args;
+  __device__ void init(int BN, int* st) {
     status = st;
     Kb = a.K / kBlockK;
     num_n = ceil_div(a.N, BN);
@@ -179,11 +188,6 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
 
-  Scheduler sched;
-  sched.init(args, BN, status);
-  if (sched.total == 0 || args.K <= 0) return;  // uniform across the CTA
-  const int Kb = sched.Kb;
-
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full_bar[s], 1);
@@ -208,15 +212,20 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem_base = *tmem_holder;
 
+  const uint32_t tmem_base = *tmem_holder;
+  const Scheduler sched(args, BN, status);
+  const int Kb = sched.Kb;
   auto fail = [&]() {
     *abort_flag = 1;
     raise_status(status, FP8GEMM_ERR_TIMEOUT);
   };
 
+  // Register budgets change at the top of each role (setmaxnreg, per
+  // warpgroup): the producer warpgroup gives registers to the promotion ones.
   if (warp == Cfg::kTmaWarp) {
     // ------------------------------------------------------ TMA producer
+    regs_decrease<Cfg::kLowRegs>();
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
@@ -242,6 +251,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     }
   } else if (warp == Cfg::kMmaWarp) {
     // ------------------------------------------------------ MMA issuer
+    regs_decrease<Cfg::kLowRegs>();
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_e4m3_f32(kBlockM, BN);
       const uint32_t a_base = smem_addr(smA);
@@ -279,8 +289,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         drain_wait(drain_bar, 0);
       }
     }
-  } else {
+  } else if (warp < Cfg::kPromoWarps) {
     // ------------------------------------------ promotion + epilogue
+    regs_increase<Cfg::kHighRegs>();
     const int wg = warp / 4;                 // column half
     const int row = (warp % 4) * 32 + lane;  // TMEM lane = tile row
     const uint32_t lane_base = uint32_t((warp % 4) * 32) << 16;
@@ -296,9 +307,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       const float* sa_ptr = args.sA + size_t(tile.row0 + row) * Kb;
       const float* sb_ptr = args.sB + (size_t(tile.e) * Nb + col0 / kBlockK) * Kb;
 
-      float acc[Cfg::kColsPerWG];
+      // FP32 accumulator, two columns per float2 so the promotion runs on the
+      // packed FMA (FFMA2)
+      float2 acc[Cfg::kColsPerWG / 2];
 #pragma unroll
-      for (int j = 0; j < Cfg::kColsPerWG; ++j) acc[j] = 0.f;
+      for (int j = 0; j < Cfg::kColsPerWG / 2; ++j) acc[j] = make_float2(0.f, 0.f);
 
       float sa_next = row_ok ? __ldg(sa_ptr) : 0.f;
       float sb_next = cols_ok ? __ldg(sb_ptr) : 0.f;
@@ -317,17 +330,36 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         }
         tc_fence_after();
         const uint32_t taddr = tmem_base + lane_base + buf * BN + wg * Cfg::kColsPerWG;
+        const float2 sc2 = make_float2(sc, sc);
+        // 16-column chunks, double-buffered: the load of chunk c+1 is in
+        // flight while chunk c is scaled and added; the TMEM buffer goes back
+        // to the MMA warp as soon as the last chunk has landed in registers.
+        constexpr int kChunks = Cfg::kColsPerWG / 16;
+        uint32_t ra[16], rb[16];
+        auto release = [&]() {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty_bar[buf]);
+        };
+        auto promote = [&](const uint32_t(&r)[16], int c) {
 #pragma unroll
-        for (int c = 0; c < Cfg::kColsPerWG / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(taddr + c * 32, r);
-          tmem_ld_wait();
+          for (int j = 0; j < 8; ++j) {
+            const float2 p = make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+            acc[c * 8 + j] = __ffma2_rn(p, sc2, acc[c * 8 + j]);
+          }
+        };
+        tmem_ld_32x32b_x16(taddr, ra);
+        tmem_ld_wait_tied16(ra);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) acc[c * 32 + j] = fmaf(__uint_as_float(r[j]), sc, acc[c * 32 + j]);
+        for (int c = 0; c < kChunks; c += 2) {
+          tmem_ld_32x32b_x16(taddr + (c + 1) * 16, rb);
+          promote(ra, c);
+          tmem_ld_wait_tied16(rb);
+          if (c + 2 == kChunks) release();
+          if (c + 2 < kChunks) tmem_ld_32x32b_x16(taddr + (c + 2) * 16, ra);
+          promote(rb, c + 1);
+          if (c + 2 < kChunks) tmem_ld_wait_tied16(ra);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty_bar[buf]);
       }
       if (!ok) break;
       // epilogue: BF16 (round to nearest even), 16-byte stores
@@ -337,10 +369,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         for (int j = 0; j < Cfg::kColsPerWG; j += 8) {
           if (col0 + j < args.N) {
             uint4 v;
-            __nv_bfloat162 p0 = __floats2bfloat162_rn(acc[j + 0], acc[j + 1]);
-            __nv_bfloat162 p1 = __floats2bfloat162_rn(acc[j + 2], acc[j + 3]);
-            __nv_bfloat162 p2 = __floats2bfloat162_rn(acc[j + 4], acc[j + 5]);
-            __nv_bfloat162 p3 = __floats2bfloat162_rn(acc[j + 6], acc[j + 7]);
+            __nv_bfloat162 p0 = __float22bfloat162_rn(acc[j / 2 + 0]);
+            __nv_bfloat162 p1 = __float22bfloat162_rn(acc[j / 2 + 1]);
+            __nv_bfloat162 p2 = __float22bfloat162_rn(acc[j / 2 + 2]);
+            __nv_bfloat162 p3 = __float22bfloat162_rn(acc[j / 2 + 3]);
             v.x = *reinterpret_cast<uint32_t*>(&p0);
             v.y = *reinterpret_cast<uint32_t*>(&p1);
             v.z = *reinterpret_cast<uint32_t*>(&p2);
@@ -350,6 +382,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         }
       }
     }
+  } else {
+    regs_decrease<Cfg::kLowRegs>();  // warps 10-11: no work
   }
 
   __syncthreads();
