@@ -25,6 +25,7 @@ ERR_ARCH = -4
 ERR_LAUNCH = -5
 ERR_DEVICE_STATUS = -6
 ERR_TIMEOUT = -7
+ERR_SCRATCH_LIMIT = -8
 
 _lib = None
 _lock = threading.Lock()
@@ -38,6 +39,7 @@ SIGNATURES = [
     ("fp8gemm_dense", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _P]),
     ("fp8gemm_grouped_contiguous", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     ("fp8gemm_grouped_masked", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
+    ("fp8gemm_dense_small_m_noalloc", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _P]),
     ("fp8gemm_get_device_status", _I, [_P, ctypes.POINTER(ctypes.c_int)]),
     ("fp8gemm_strerror", ctypes.c_char_p, [_I]),
     ("fp8gemm_num_kernel_launches", ctypes.c_uint64, []),
@@ -208,6 +210,20 @@ def fp8gemm_grouped_masked(A, sA, B, sB, masked_m, D=None, stream=None):
         _ptr(A), _ptr(_f32(sA, "sA")), _ptr(B), _ptr(_f32(sB, "sB")),
         _ptr(_i32(masked_m, "masked_m")), _ptr(_dev(D, "D")), E, M_max, N, K,
         _stream(stream)), "fp8gemm_grouped_masked")
+    return D
+
+
+def fp8gemm_dense_small_m_noalloc(A, sA, B, sB, D, stream=None):
+    """fp8gemm_dense for M <= 64 without any device allocation by the library:
+    the caller provides D, and the split-K scratch is a fixed array inside the
+    library (shared by every call on the device; calls must not overlap on the
+    GPU)."""
+    A, B = _u8(A, "A"), _u8(B, "B")
+    M, K = A.shape
+    N = B.shape[0]
+    _check(lib().fp8gemm_dense_small_m_noalloc(
+        _ptr(A), _ptr(_f32(sA, "sA")), _ptr(B), _ptr(_f32(sB, "sB")), _ptr(_dev(D, "D")),
+        M, N, K, _stream(stream)), "fp8gemm_dense_small_m_noalloc")
     return D
 
 

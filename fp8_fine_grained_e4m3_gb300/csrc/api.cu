@@ -158,6 +158,11 @@ int ctx_for(cudaStream_t stream, LaunchCtx* c) {
 
 }  // namespace
 
+namespace fp8gemm {
+int make_launch_ctx(cudaStream_t stream, LaunchCtx* c) { return ctx_for(stream, c); }
+void count_kernel_launches(int n) { g_launches += n; }
+}  // namespace fp8gemm
+
 extern "C" {
 
 int fp8_quant_1x128(const float* X, uint8_t* Q, float* sX, int M, int K,
@@ -265,6 +270,8 @@ const char* fp8gemm_strerror(int code) {
     case FP8GEMM_ERR_LAUNCH: return "CUDA launch or runtime call failed";
     case FP8GEMM_ERR_DEVICE_STATUS: return "device-side input error (expert index or row count)";
     case FP8GEMM_ERR_TIMEOUT: return "a pipeline wait exceeded its time limit";
+    case FP8GEMM_ERR_SCRATCH_LIMIT:
+      return "problem exceeds the fixed scratch of fp8gemm_dense_small_m_noalloc (M <= 64)";
     default: return "unknown status";
   }
 }

@@ -58,6 +58,12 @@ cudaError_t launch_gemm_small_m(const LaunchCtx& c, const GemmArgs& a, void* wor
                                 size_t workspace_bytes);
 size_t small_m_workspace_bytes(int num_sms, int N);
 
+// Fills `c` for the current device and `stream` (SM count, status word);
+// returns an fp8gemm_status code.  Defined in api.cu.
+int make_launch_ctx(cudaStream_t stream, LaunchCtx* c);
+// Adds to the host-side count of kernels enqueued.  Defined in api.cu.
+void count_kernel_launches(int n);
+
 // Encodes a 2-D K-major uint8 tensor map with 128-byte swizzling:
 // rows x cols bytes, box of box_rows x 128 bytes.  Defined in api.cu.
 bool make_tmap_u8_sw128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,

@@ -62,7 +62,8 @@ enum fp8gemm_status {
   FP8GEMM_ERR_ARCH = -4,
   FP8GEMM_ERR_LAUNCH = -5,
   FP8GEMM_ERR_DEVICE_STATUS = -6,
-  FP8GEMM_ERR_TIMEOUT = -7
+  FP8GEMM_ERR_TIMEOUT = -7,
+  FP8GEMM_ERR_SCRATCH_LIMIT = -8
 };
 
 /*
@@ -139,6 +140,37 @@ int fp8gemm_grouped_contiguous(const uint8_t* A, const float* sA, const uint8_t*
 int fp8gemm_grouped_masked(const uint8_t* A, const float* sA, const uint8_t* B,
                            const float* sB, const int32_t* masked_m, void* D,
                            int E, int M_max, int N, int K, fp8gemm_stream_t stream);
+
+/*
+ * fp8gemm_dense_small_m_noalloc -- the same computation as fp8gemm_dense for
+ * decode-sized M (1..64), for callers that must not have the library allocate
+ * device memory: a server that reserves its whole memory budget up front and
+ * treats any later allocation as an error, a framework whose own pool owns the
+ * device memory, or a latency-critical loop that cannot take cudaMalloc's
+ * implicit synchronisation.  (The pages this library follows have no
+ * counterpart; this variant exists for that constraint only.)
+ *
+ * It allocates nothing: its split-K scratch is a fixed array of about
+ * 10.3 MiB in the library's device image, present on every GPU that loads the
+ * library until the process exits.  The first call on each device does a
+ * one-time set-up -- it looks up that array's device address with
+ * cudaGetSymbolAddress -- and later calls reuse it; make that first call on
+ * each device before any CUDA stream capture begins.
+ *
+ * Arguments, layouts, ownership and results are those of fp8gemm_dense, with
+ * these limits: M <= 64 and N <= 8388608 (ceil(N/128) arrival counters must
+ * fit), at most 160 SMs used.  Larger problems return
+ * FP8GEMM_ERR_SCRATCH_LIMIT and enqueue nothing.
+ *
+ * All calls on a device share the one scratch array and it keeps the previous
+ * call's contents; each call clears what must start at zero with an
+ * asynchronous memset on `stream`.  Calls whose execution overlaps on the GPU
+ * (e.g. issued on two streams without ordering between them) race on the
+ * scratch and produce wrong results: order them.
+ */
+int fp8gemm_dense_small_m_noalloc(const uint8_t* A, const float* sA, const uint8_t* B,
+                                  const float* sB, void* D, int M, int N, int K,
+                                  fp8gemm_stream_t stream);
 
 /*
  * fp8gemm_get_device_status -- synchronise `stream`, then read and clear the
