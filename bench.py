@@ -109,6 +109,24 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------- GPU arm
+def max_over_ranks(x, world):
+    """The slowest rank's value (replicas are timed separately; the job is as
+    slow as its slowest GPU).  Works on NCCL (CUDA tensor) and gloo (CPU)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_tflops(flops_per_rank_step, ms_per_step, world):
+    """Whole-job throughput: every rank does the same step (weak scaling)."""
+    return world * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
 def gemm_bytes(M, N, K, e_active=1, rows=None):
     """Algorithmic bytes of one block-scaled GEMM: A and its scales for the
     real rows, B and its scales for the active experts, D for the real rows."""
@@ -191,11 +209,8 @@ def run_gpu(args, rank, world):
     ms_per_step = sum(step_ms) / K_steps
     gemm_ms = [sum(g[j][0].elapsed_time(g[j][1]) for g in gev) / K_steps
                for j in range(len(cases))]
-    if world > 1:
-        t = torch.tensor([ms_per_step], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_per_step = float(t.item())
-    value = world * flops_step / (ms_per_step * 1e-3) / 1e12
+    ms_per_step = max_over_ranks(ms_per_step, world)
+    value = aggregate_tflops(flops_step, ms_per_step, world)
 
     # roofline of the dominant kernel: the dense GEMM on the 4096x7168x16384
     # shape (about 80 % of the step); the other shape is listed beside it

@@ -13,9 +13,16 @@
 //   N/128 is far below the SM count ("news.rkmt.cn/news/5092" sections 1.2
 //   and 4.2: with M of 1-16, fixed tiles leave most SMs idle; size the work
 //   to the SM count).  A CTA whose range ends inside a tile leaves its FP32
-//   partial in a workspace slot; the last CTA to finish a tile (atomic
-//   counter) sums every contributor's partial in CTA order -- a fixed order,
-//   so the result is deterministic -- writes BF16 and resets the counter.
+//   partial in a workspace slot; the last CTA to finish a tile (one
+//   acquire-release atomic per CTA) sums every contributor's partial in CTA
+//   order -- a fixed order, so results are deterministic -- writes BF16 and
+//   resets the tile's counter for the next launch.
+// * Programmatic dependent launch: the prologue and an L2 prefetch of the
+//   CTA's weight tiles run while the previous kernel in the stream finishes;
+//   every load into shared memory, and every access to activations, scales,
+//   the workspace and D, waits for it (griddepcontrol.wait).  Shared memory
+//   and registers are sized so that two CTAs fit on one SM during that
+//   overlap.
 //
 // CTA layout (192 threads): warps 0-3 promotion/epilogue (thread = TMEM lane
 // = output column), warp 4 TMA producer, warp 5 MMA issuer.
@@ -25,24 +32,26 @@
 namespace fp8gemm {
 namespace {
 
-constexpr int kSmStages = 8;
 constexpr int kCounterBytes = 256 * 1024;  // one int per N tile: N <= 8M columns
 constexpr int kMaxMP = 64;
 
 template <int MP_>
 struct SmCfg {
   static constexpr int MP = MP_;
-  static constexpr int kStages = kSmStages;
+  // stages: as many as keep two CTAs within one SM's shared memory
+  static constexpr int kStages = MP == 16 ? 6 : (MP == 32 ? 5 : 4);
   static constexpr int kThreads = 192;
   static constexpr int kTmaWarp = 4;
   static constexpr int kMmaWarp = 5;
   static constexpr int kWBytes = 128 * kBlockK;  // weight tile: 16 KB
   static constexpr int kXBytes = MP * kBlockK;   // activation tile
   static constexpr int kTmemCols = 2 * MP < 32 ? 32 : 2 * MP;
-  static constexpr int kAuxBytes = 1024;
+  static constexpr int kScaleKb = 16;  // K blocks of scales staged per batch
+  static constexpr int kAuxBytes = 256 + kScaleKb * (MP + 4) * 4;
   static constexpr size_t kSmemBytes =
       1024 + size_t(kStages) * (kWBytes + kXBytes) + kAuxBytes;
   static_assert(MP == 16 || MP == 32 || MP == 64, "MP");
+  static_assert(kSmemBytes <= 113 * 1024, "two CTAs per SM");
 };
 
 struct StreamK {
@@ -60,7 +69,7 @@ __device__ __forceinline__ void drain_wait_sm(uint64_t* bar, uint32_t parity) {
 }
 
 template <class Cfg>
-__global__ void __launch_bounds__(Cfg::kThreads, 1)
+__global__ void __launch_bounds__(Cfg::kThreads, 2)
     gemm_small_m_kernel(const __grid_constant__ CUtensorMap tmW,
                         const __grid_constant__ CUtensorMap tmX, const GemmArgs args,
                         float* ws_partials, int* ws_counters, int* status) {
@@ -78,18 +87,22 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   uint64_t* tfull_bar = full_bar + 2 * kStages;
   uint64_t* tempty_bar = full_bar + 2 * kStages + 2;
   uint64_t* drain_bar = full_bar + 2 * kStages + 4;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(full_bar + 2 * kStages + 5);
+  uint64_t* group_bar = full_bar + 2 * kStages + 5;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(full_bar + 2 * kStages + 6);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_holder + 2);
-  uint64_t* group_bar = full_bar + 2 * kStages + 7;
+  // scales of the current batch of K blocks: sa_s[q][j] = sA[j, kb + q], sb_s[q]
+  float* sa_s = reinterpret_cast<float*>(aux + 256);
+  float* sb_s = sa_s + Cfg::kScaleKb * MP;
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const int Kb = args.K / kBlockK;
   const int n_tiles = ceil_div(args.N, 128);
-  StreamK sk{(long long)n_tiles * Kb, int(gridDim.x), Kb};
+  const StreamK sk{(long long)n_tiles * Kb, int(gridDim.x), Kb};
   const long long u_begin = sk.begin(blockIdx.x);
   const long long u_end = sk.begin(blockIdx.x + 1);
+  const int n_units = int(u_end - u_begin);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -117,6 +130,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  // the next kernel in the stream may start its own prologue now
+  griddep_launch_dependents();
 
   auto fail = [&]() {
     *abort_flag = 1;
@@ -124,70 +139,65 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   };
 
   if (warp == Cfg::kTmaWarp) {
+    // ------------------------------------------------------ TMA producer
     if (lane == 0) {
       const uint64_t pol_stream = l2_policy_evict_first();  // weights: read once
       const uint64_t pol_keep = l2_policy_evict_last();     // activations: read by all
-      uint32_t it = 0;
-      bool ok = true;
-      for (long long u = u_begin; u < u_end && ok;) {
-        const int tile = int(u / Kb);
-        const int kb0 = int(u % Kb);
-        const int kb1 = int(min((long long)Kb, kb0 + (u_end - u)));
-        for (int kb = kb0; kb < kb1; ++kb, ++it) {
-          const int s = it % kStages;
-          const uint32_t ph = (it / kStages) & 1;
-          if (!mbar_wait(&empty_bar[s], ph ^ 1, abort_flag)) {
-            fail();
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&full_bar[s], Cfg::kWBytes + Cfg::kXBytes);
-          tma_load_2d_hint(smW + s * Cfg::kWBytes, &tmW, &full_bar[s], kb * kBlockK, tile * 128,
-                           pol_stream);
-          tma_load_2d_hint(smX + s * Cfg::kXBytes, &tmX, &full_bar[s], kb * kBlockK, 0,
-                           pol_keep);
-        }
-        u += kb1 - kb0;
+      // Pull this CTA's weight tiles towards L2 while the previous kernel in
+      // the stream may still be running (a prefetch cannot return stale data);
+      // every load into shared memory waits for that kernel.
+      for (int i = 0; i < n_units; ++i) {
+        const long long u = u_begin + i;
+        tma_prefetch_l2_2d(&tmW, int(u % Kb) * kBlockK, int(u / Kb) * 128);
       }
-      const uint32_t n = it < uint32_t(kStages) ? it : uint32_t(kStages);
-      for (uint32_t i = it - n; i < it; ++i)
-        drain_wait_sm(&full_bar[i % kStages], (i / kStages) & 1);
+      griddep_wait();
+      int i = 0;
+      for (; i < n_units; ++i) {
+        const long long u = u_begin + i;
+        const int s = i % kStages;
+        const uint32_t ph = (i / kStages) & 1;
+        if (!mbar_wait(&empty_bar[s], ph ^ 1, abort_flag)) {
+          fail();
+          break;
+        }
+        mbar_arrive_expect_tx(&full_bar[s], Cfg::kWBytes + Cfg::kXBytes);
+        tma_load_2d_hint(smW + s * Cfg::kWBytes, &tmW, &full_bar[s], int(u % Kb) * kBlockK,
+                         int(u / Kb) * 128, pol_stream);
+        tma_load_2d_hint(smX + s * Cfg::kXBytes, &tmX, &full_bar[s], int(u % Kb) * kBlockK, 0,
+                         pol_keep);
+      }
+      const int n = i < kStages ? i : kStages;  // let in-flight copies land
+      for (int j = i - n; j < i; ++j) drain_wait_sm(&full_bar[j % kStages], (j / kStages) & 1);
     }
   } else if (warp == Cfg::kMmaWarp) {
+    // ------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_e4m3_f32(128, MP);
       const uint32_t w_base = smem_addr(smW);
       const uint32_t x_base = smem_addr(smX);
-      uint32_t it = 0;
-      bool ok = true;
-      for (long long u = u_begin; u < u_end && ok;) {
-        const int kb0 = int(u % Kb);
-        const int kb1 = int(min((long long)Kb, kb0 + (u_end - u)));
-        for (int kb = kb0; kb < kb1; ++kb, ++it) {
-          const int s = it % kStages;
-          const uint32_t ph = (it / kStages) & 1;
-          const int buf = it & 1;
-          const uint32_t tph = (it >> 1) & 1;
-          if (!mbar_wait(&tempty_bar[buf], tph ^ 1, abort_flag) ||
-              !mbar_wait(&full_bar[s], ph, abort_flag)) {
-            fail();
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t d_tmem = tmem_base + buf * MP;
-#pragma unroll
-          for (int k = 0; k < kBlockK / 32; ++k) {
-            const uint64_t ad = smem_desc_sw128_kmajor(w_base + s * Cfg::kWBytes + k * 32);
-            const uint64_t bd = smem_desc_sw128_kmajor(x_base + s * Cfg::kXBytes + k * 32);
-            umma_e4m3(d_tmem, ad, bd, idesc, k > 0 ? 1u : 0u);
-          }
-          umma_commit(&empty_bar[s]);
-          umma_commit(&tfull_bar[buf]);
+      int i = 0;
+      for (; i < n_units; ++i) {
+        const int s = i % kStages;
+        const uint32_t ph = (i / kStages) & 1;
+        const int buf = i & 1;
+        const uint32_t tph = (i >> 1) & 1;
+        if (!mbar_wait(&tempty_bar[buf], tph ^ 1, abort_flag) ||
+            !mbar_wait(&full_bar[s], ph, abort_flag)) {
+          fail();
+          break;
         }
-        u += kb1 - kb0;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * MP;
+#pragma unroll
+        for (int k = 0; k < kBlockK / 32; ++k) {
+          const uint64_t ad = smem_desc_sw128_kmajor(w_base + s * Cfg::kWBytes + k * 32);
+          const uint64_t bd = smem_desc_sw128_kmajor(x_base + s * Cfg::kXBytes + k * 32);
+          umma_e4m3(d_tmem, ad, bd, idesc, k > 0 ? 1u : 0u);
+        }
+        umma_commit(&empty_bar[s]);
+        umma_commit(&tfull_bar[buf]);
       }
-      if (it > 0) {
+      if (i > 0) {  // every issued MMA has finished before TMEM is released
         umma_commit(drain_bar);
         drain_wait_sm(drain_bar, 0);
       }
@@ -198,7 +208,6 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     const uint32_t lane_base = uint32_t(warp * 32) << 16;
     const int M = args.M;
     const int first_tile = int(u_begin / Kb);
-    uint32_t it = 0;
     uint32_t gphase = 0;
     bool ok = true;
     // bounded barrier over the 128 promotion threads
@@ -208,23 +217,31 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       gphase ^= 1;
       return r;
     };
+    griddep_wait();  // sA, the workspace and D belong to the stream's order
+    int it = 0;
     for (long long u = u_begin; u < u_end && ok;) {
       const int tile = int(u / Kb);
       const int kb0 = int(u % Kb);
       const int kb1 = int(min((long long)Kb, kb0 + (u_end - u)));
-      const float* sb_ptr = args.sB + size_t(tile) * Kb;
 
       float acc[MP];
 #pragma unroll
       for (int j = 0; j < MP; ++j) acc[j] = 0.f;
 
       for (int kb = kb0; kb < kb1; ++kb, ++it) {
-        // scale product of column j (activation row j) for this K block; the
-        // loads are warp-uniform broadcasts
-        float sc[MP];
-        const float sb = __ldg(sb_ptr + kb);
-#pragma unroll
-        for (int j = 0; j < MP; ++j) sc[j] = j < M ? __ldg(args.sA + size_t(j) * Kb + kb) * sb : 0.f;
+        const int q = (kb - kb0) % Cfg::kScaleKb;
+        if (q == 0) {
+          // stage the scales of the next batch of K blocks with independent
+          // loads (one latency per batch, not one per K block)
+          const int nkb = min(Cfg::kScaleKb, kb1 - kb);
+          if (!group_sync()) { fail(); ok = false; break; }  // previous batch consumed
+          for (int idx = t; idx < MP * nkb; idx += 128) {
+            const int j = idx / nkb, qq = idx % nkb;
+            sa_s[qq * MP + j] = j < M ? __ldg(args.sA + size_t(j) * Kb + kb + qq) : 0.f;
+          }
+          if (t < nkb) sb_s[t] = __ldg(args.sB + size_t(tile) * Kb + kb + t);
+          if (!group_sync()) { fail(); ok = false; break; }
+        }
         const int buf = it & 1;
         const uint32_t tph = (it >> 1) & 1;
         if (!mbar_wait(&tfull_bar[buf], tph, abort_flag)) {
@@ -234,26 +251,45 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         }
         tc_fence_after();
         const uint32_t taddr = tmem_base + lane_base + buf * MP;
+        const float sb = sb_s[q];
+        const float* sa_row = sa_s + q * MP;
         if constexpr (MP == 16) {
           uint32_t r[16];
           tmem_ld_32x32b_x16(taddr, r);
-          tmem_ld_wait();
+          tmem_ld_wait_tied16(r);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty_bar[buf]);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) acc[j] = fmaf(__uint_as_float(r[j]), sc[j], acc[j]);
+          for (int j = 0; j < 16; j += 4) {
+            const float4 a4 = *reinterpret_cast<const float4*>(sa_row + j);
+            acc[j] = fmaf(__uint_as_float(r[j]), a4.x * sb, acc[j]);
+            acc[j + 1] = fmaf(__uint_as_float(r[j + 1]), a4.y * sb, acc[j + 1]);
+            acc[j + 2] = fmaf(__uint_as_float(r[j + 2]), a4.z * sb, acc[j + 2]);
+            acc[j + 3] = fmaf(__uint_as_float(r[j + 3]), a4.w * sb, acc[j + 3]);
+          }
         } else {
 #pragma unroll
           for (int c = 0; c < MP / 32; ++c) {
             uint32_t r[32];
             tmem_ld_32x32b_x32(taddr + c * 32, r);
-            tmem_ld_wait();
+            tmem_ld_wait_tied(r);
+            if (c + 1 == MP / 32) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&tempty_bar[buf]);
+            }
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              acc[c * 32 + j] = fmaf(__uint_as_float(r[j]), sc[c * 32 + j], acc[c * 32 + j]);
+            for (int j = 0; j < 32; j += 4) {
+              const float4 a4 = *reinterpret_cast<const float4*>(sa_row + c * 32 + j);
+              const int o = c * 32 + j;
+              acc[o] = fmaf(__uint_as_float(r[j]), a4.x * sb, acc[o]);
+              acc[o + 1] = fmaf(__uint_as_float(r[j + 1]), a4.y * sb, acc[o + 1]);
+              acc[o + 2] = fmaf(__uint_as_float(r[j + 2]), a4.z * sb, acc[o + 2]);
+              acc[o + 3] = fmaf(__uint_as_float(r[j + 3]), a4.w * sb, acc[o + 3]);
+            }
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty_bar[buf]);
       }
       if (!ok) break;
 
@@ -261,18 +297,18 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       const bool col_ok = n < args.N;
       bool write = true;
       if (!(kb0 == 0 && kb1 == Kb)) {
-        // split tile: publish this CTA's partial, the last contributor reduces
+        // split tile: publish this CTA's partial; the last contributor reduces
         const int slot_idx = 2 * blockIdx.x + (tile == first_tile ? 0 : 1);
         float* mine = ws_partials + size_t(slot_idx) * MP * 128;
 #pragma unroll
         for (int j = 0; j < MP; ++j) mine[j * 128 + t] = acc[j];
-        __threadfence();
         if (!group_sync()) { fail(); ok = false; break; }
         const int c_first = sk.cta_of((long long)tile * Kb);
         const int c_last = sk.cta_of((long long)(tile + 1) * Kb - 1);
         if (t == 0) {
-          __threadfence();
-          const int prev = atomicAdd(ws_counters + tile, 1);
+          // release this CTA's partial (ordered before by the group barrier),
+          // acquire the partials of the CTAs that arrived earlier
+          const int prev = atomic_add_acq_rel_gpu(ws_counters + tile, 1);
           const int is_last = prev == c_last - c_first;
           if (is_last) ws_counters[tile] = 0;  // ready for the next launch
           *last_flag = is_last;
@@ -281,7 +317,6 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         write = *last_flag != 0;
         if (!group_sync()) { fail(); ok = false; break; }  // last_flag is reused
         if (write) {
-          __threadfence();
 #pragma unroll
           for (int j = 0; j < MP; ++j) acc[j] = 0.f;
           for (int c = c_first; c <= c_last; ++c) {
@@ -333,9 +368,18 @@ cudaError_t run(const LaunchCtx& c, const GemmArgs& a, void* ws, size_t ws_bytes
   }
   int* counters = reinterpret_cast<int*>(ws);
   float* partials = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kCounterBytes);
-  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, c.stream>>>(tmW, tmX, a, partials, counters,
-                                                            c.status);
-  return cudaGetLastError();
+  // launched as a programmatic dependent of the previous kernel in the stream
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(Cfg::kThreads);
+  cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+  cfg.stream = c.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tmW, tmX, a, partials, counters, c.status);
 }
 
 }  // namespace

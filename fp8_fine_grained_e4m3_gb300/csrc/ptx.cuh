@@ -106,6 +106,17 @@ __device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* m
       : "memory");
 }
 
+// Prefetch one tile of a tensor map into L2 (no shared memory, no barrier).
+// Safe to issue before the data's producer has finished: L2 is the point of
+// coherence, so later writes still reach whoever reads the line afterwards.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t c0,
+                                                   int32_t c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1)
+               : "memory");
+}
+
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -259,6 +270,34 @@ __device__ __forceinline__ void regs_increase() {
 template <uint32_t kRegs>
 __device__ __forceinline__ void regs_decrease() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
+// ------------------------------------------- programmatic dependent launch
+// Wait until the grids this one depends on (in stream order) have completed
+// and their memory is visible.  A no-op when the launch has no such
+// dependency.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the next grid in the stream, if it was launched as a programmatic
+// dependent, to start its own prologue now.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Device-scope atomic add with acquire-release semantics (returns the old
+// value): publishes what this thread -- and, through a preceding CTA barrier,
+// its CTA -- wrote before it, and sees what earlier releasers published.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int* p, int v) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
 }
 
 // Named barrier over `nthreads` threads (a multiple of 32), id 1..15.
