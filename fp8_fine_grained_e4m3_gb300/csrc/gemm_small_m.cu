@@ -45,12 +45,17 @@ struct SmCfg {
   static constexpr int kMmaWarp = 5;
   static constexpr int kWBytes = 128 * kBlockK;  // weight tile: 16 KB
   static constexpr int kXBytes = MP * kBlockK;   // activation tile
-  static constexpr int kTmemCols = 2 * MP < 32 ? 32 : 2 * MP;
+  // TMEM partial buffers: enough that the MMA never waits for promotion on
+  // the few K blocks a CTA handles (a partial is only MP columns)
+  static constexpr int kTmemBufs = MP == 64 ? 4 : 8;
+  static constexpr int kTmemCols = kTmemBufs * MP;  // 128 or 256: two CTAs fit in 512
   static constexpr int kScaleKb = 16;  // K blocks of scales staged per batch
-  static constexpr int kAuxBytes = 256 + kScaleKb * (MP + 4) * 4;
+  static constexpr int kBarBytes = 512;
+  static constexpr int kAuxBytes = kBarBytes + kScaleKb * (MP + 4) * 4;
   static constexpr size_t kSmemBytes =
       1024 + size_t(kStages) * (kWBytes + kXBytes) + kAuxBytes;
   static_assert(MP == 16 || MP == 32 || MP == 64, "MP");
+  static_assert((2 * kStages + 2 * kTmemBufs + 4) * 8 + 16 <= kBarBytes, "barrier area");
   static_assert(kSmemBytes <= 113 * 1024, "two CTAs per SM");
 };
 
@@ -84,15 +89,16 @@ __global__ void __launch_bounds__(Cfg::kThreads, 2)
   uint8_t* aux = smX + kStages * Cfg::kXBytes;
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(aux);
   uint64_t* empty_bar = full_bar + kStages;
+  constexpr int NB = Cfg::kTmemBufs;
   uint64_t* tfull_bar = full_bar + 2 * kStages;
-  uint64_t* tempty_bar = full_bar + 2 * kStages + 2;
-  uint64_t* drain_bar = full_bar + 2 * kStages + 4;
-  uint64_t* group_bar = full_bar + 2 * kStages + 5;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(full_bar + 2 * kStages + 6);
+  uint64_t* tempty_bar = tfull_bar + NB;
+  uint64_t* drain_bar = tempty_bar + NB;
+  uint64_t* group_bar = drain_bar + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(group_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_holder + 2);
   // scales of the current batch of K blocks: sa_s[q][j] = sA[j, kb + q], sb_s[q]
-  float* sa_s = reinterpret_cast<float*>(aux + 256);
+  float* sa_s = reinterpret_cast<float*>(aux + Cfg::kBarBytes);
   float* sb_s = sa_s + Cfg::kScaleKb * MP;
 
   const int warp = threadIdx.x / 32;
@@ -109,7 +115,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 2)
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NB; ++b) {
       mbar_init(&tfull_bar[b], 1);
       mbar_init(&tempty_bar[b], 4);
     }
@@ -179,8 +185,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 2)
       for (; i < n_units; ++i) {
         const int s = i % kStages;
         const uint32_t ph = (i / kStages) & 1;
-        const int buf = i & 1;
-        const uint32_t tph = (i >> 1) & 1;
+        const int buf = i % NB;
+        const uint32_t tph = (i / NB) & 1;
         if (!mbar_wait(&tempty_bar[buf], tph ^ 1, abort_flag) ||
             !mbar_wait(&full_bar[s], ph, abort_flag)) {
           fail();
@@ -242,8 +248,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 2)
           if (t < nkb) sb_s[t] = __ldg(args.sB + size_t(tile) * Kb + kb + t);
           if (!group_sync()) { fail(); ok = false; break; }
         }
-        const int buf = it & 1;
-        const uint32_t tph = (it >> 1) & 1;
+        const int buf = it % NB;
+        const uint32_t tph = (it / NB) & 1;
         if (!mbar_wait(&tfull_bar[buf], tph, abort_flag)) {
           fail();
           ok = false;
@@ -300,8 +306,14 @@ __global__ void __launch_bounds__(Cfg::kThreads, 2)
         // split tile: publish this CTA's partial; the last contributor reduces
         const int slot_idx = 2 * blockIdx.x + (tile == first_tile ? 0 : 1);
         float* mine = ws_partials + size_t(slot_idx) * MP * 128;
+        if (M >= MP) {
 #pragma unroll
-        for (int j = 0; j < MP; ++j) mine[j * 128 + t] = acc[j];
+          for (int j = 0; j < MP; ++j) mine[j * 128 + t] = acc[j];
+        } else {  // only the M real rows are published
+#pragma unroll
+          for (int j = 0; j < MP; ++j)
+            if (j < M) mine[j * 128 + t] = acc[j];
+        }
         if (!group_sync()) { fail(); ok = false; break; }
         const int c_first = sk.cta_of((long long)tile * Kb);
         const int c_last = sk.cta_of((long long)(tile + 1) * Kb - 1);
@@ -317,13 +329,21 @@ __global__ void __launch_bounds__(Cfg::kThreads, 2)
         write = *last_flag != 0;
         if (!group_sync()) { fail(); ok = false; break; }  // last_flag is reused
         if (write) {
+          // sum every contributor's partial in CTA order (fixed order:
+          // deterministic); only the M real rows were published
 #pragma unroll
           for (int j = 0; j < MP; ++j) acc[j] = 0.f;
           for (int c = c_first; c <= c_last; ++c) {
             const int cs = int(sk.begin(c) / Kb) == tile ? 2 * c : 2 * c + 1;
             const float* p = ws_partials + size_t(cs) * MP * 128;
+            if (M >= MP) {
 #pragma unroll
-            for (int j = 0; j < MP; ++j) acc[j] += __ldcg(p + j * 128 + t);
+              for (int j = 0; j < MP; ++j) acc[j] += __ldcg(p + j * 128 + t);
+            } else {
+#pragma unroll
+              for (int j = 0; j < MP; ++j)
+                if (j < M) acc[j] += __ldcg(p + j * 128 + t);
+            }
           }
         }
       }
