@@ -583,6 +583,7 @@ def run_kernel_case(name, reps):
     else:
         raise SystemExit(f"unknown kernel case {name}")
     torch.cuda.synchronize()
+    torch.cuda.empty_cache()  # keep the device footprint small for profilers
     for _ in range(reps):
         fn()
     torch.cuda.synchronize()
