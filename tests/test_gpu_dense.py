@@ -3,7 +3,7 @@
 import numpy as np
 import pytest
 
-from tests.gpu_helpers import (assert_close, dev, host, ogemm, quantised_dense,
+from tests.gpu_helpers import (assert_close, dev, host, ogemm, oquant, quantised_dense,
                                sample_rows_cols)
 
 pytestmark = pytest.mark.gpu
@@ -77,3 +77,25 @@ def test_prefill_full_size_sampled(M, N, K):
     ref = ogemm.gemm_dense_at(A, sA, B, sB, rows, cols)
     assert_close(got[rows][:, cols], ref, f"prefill {M}x{N}x{K}")
     assert np.isfinite(got).all()
+
+
+@pytest.mark.parametrize("M,N,K", [(4, 2048, 1024), (64, 7168, 2048), (16, 2048, 7168)])
+def test_decode_chain_without_host_sync(M, N, K):
+    """The decode GEMM is launched as a programmatic dependent of the previous
+    kernel.  Run it right after the kernels that produce its A and B, and
+    three GEMMs back to back sharing the stream's split-K workspace, with no
+    host synchronisation in between."""
+    from fp8_fine_grained_e4m3_gb300 import synthetic
+    b = _b()
+    outs, refs = [], []
+    for seed in (21, 22, 23):
+        X, W = synthetic.dense_operands(M, N, K, kind="decode", seed=seed)
+        A8, sA = b.fp8_quant_1x128(dev(X))
+        B8, sB = b.fp8_quant_128x128(dev(W))
+        outs.append(b.fp8gemm_dense(A8, sA, B8, sB))
+        Ao, sAo = oquant.quant_1x128_fast(X)
+        Bo, sBo = oquant.quant_128x128_fast(W)
+        refs.append(ogemm.gemm_dense(Ao, sAo, Bo, sBo))
+    for got, ref in zip(outs, refs):
+        assert_close(host(got), ref, f"chained decode {M}x{N}x{K}")
+    assert b.fp8gemm_get_device_status() == b.OK
