@@ -200,10 +200,11 @@ int fp8gemm_dense(const uint8_t* A, const float* sA, const uint8_t* B, const flo
   GemmArgs a{GemmMode::kDense, A, sA, B, sB, nullptr, static_cast<__nv_bfloat16*>(D),
              M, N, K, 1};
   if (M <= kSmallM) {
+    if (!small_m_uses_workspace(c, a)) return finish(launch_gemm_small_m_any(c, a, nullptr, 0), 1);
     const size_t bytes = small_m_workspace_bytes(c.num_sms, N);
     void* ws = nullptr;
     if (int r = workspace_for(stream, bytes, &ws)) return r;
-    return finish(launch_gemm_small_m(c, a, ws, bytes), 1);
+    return finish(launch_gemm_small_m_any(c, a, ws, bytes), 1);
   }
   return finish(launch_gemm_tc(c, a), 1);
 }

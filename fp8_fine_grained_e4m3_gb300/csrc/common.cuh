@@ -57,6 +57,11 @@ cudaError_t launch_gemm_tc(const LaunchCtx& c, const GemmArgs& a);
 cudaError_t launch_gemm_small_m(const LaunchCtx& c, const GemmArgs& a, void* workspace,
                                 size_t workspace_bytes);
 size_t small_m_workspace_bytes(int num_sms, int N);
+// The dense decode path: cluster split-K where it fills the SMs (no
+// workspace), stream-K through `ws` otherwise.
+bool small_m_uses_workspace(const LaunchCtx& c, const GemmArgs& a);
+cudaError_t launch_gemm_small_m_any(const LaunchCtx& c, const GemmArgs& a, void* ws,
+                                    size_t ws_bytes);
 
 // Fills `c` for the current device and `stream` (SM count, status word);
 // returns an fp8gemm_status code.  Defined in api.cu.

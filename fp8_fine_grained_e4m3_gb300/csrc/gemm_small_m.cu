@@ -17,6 +17,12 @@
 //   acquire-release atomic per CTA) sums every contributor's partial in CTA
 //   order -- a fixed order, so results are deterministic -- writes BF16 and
 //   resets the tile's counter for the next launch.
+// * Cluster split-K: when the N tiles times a split factor C <= 8 fill most
+//   SMs, the C CTAs of a thread-block cluster share one tile's K range
+//   instead; each leaves its partial in its own shared memory and, after a
+//   cluster barrier, sums a 1/C share of the tile's outputs over the C
+//   partials (distributed shared memory, CTA-rank order) and writes it.  No
+//   workspace and no atomics; the hardware co-schedules a cluster's CTAs.
 // * Programmatic dependent launch: the prologue and an L2 prefetch of the
 //   CTA's weight tiles run while the previous kernel in the stream finishes;
 //   every load into shared memory, and every access to activations, scales,
@@ -34,6 +40,7 @@ namespace {
 
 constexpr int kCounterBytes = 256 * 1024;  // one int per N tile: N <= 8M columns
 constexpr int kMaxMP = 64;
+constexpr int kMaxCluster = 16;  // CTAs sharing one tile's K range
 
 template <int MP_>
 struct SmCfg {
@@ -73,11 +80,11 @@ __device__ __forceinline__ void drain_wait_sm(uint64_t* bar, uint32_t parity) {
   }
 }
 
-template <class Cfg>
+template <class Cfg, bool kClusterSplit>
 __global__ void __launch_bounds__(Cfg::kThreads, 2)
     gemm_small_m_kernel(const __grid_constant__ CUtensorMap tmW,
                         const __grid_constant__ CUtensorMap tmX, const GemmArgs args,
-                        float* ws_partials, int* ws_counters, int* status) {
+                        float* ws_partials, int* ws_counters, int* status, int cluster) {
   constexpr int MP = Cfg::MP;
   constexpr int kStages = Cfg::kStages;
 
@@ -106,8 +113,14 @@ __global__ void __launch_bounds__(Cfg::kThreads, 2)
   const int Kb = args.K / kBlockK;
   const int n_tiles = ceil_div(args.N, 128);
   const StreamK sk{(long long)n_tiles * Kb, int(gridDim.x), Kb};
-  const long long u_begin = sk.begin(blockIdx.x);
-  const long long u_end = sk.begin(blockIdx.x + 1);
+  // units [u_begin, u_end): the stream-K range, or this CTA's part of its
+  // cluster's tile
+  const int crank = kClusterSplit ? int(cluster_ctarank()) : 0;
+  const long long ctile = (long long)(blockIdx.x / cluster) * Kb;
+  const long long u_begin =
+      kClusterSplit ? ctile + (long long)crank * Kb / cluster : sk.begin(blockIdx.x);
+  const long long u_end =
+      kClusterSplit ? ctile + (long long)(crank + 1) * Kb / cluster : sk.begin(blockIdx.x + 1);
   const int n_units = int(u_end - u_begin);
 
   if (threadIdx.x == 0) {
@@ -302,7 +315,16 @@ __global__ void __launch_bounds__(Cfg::kThreads, 2)
       const int n = tile * 128 + t;
       const bool col_ok = n < args.N;
       bool write = true;
-      if (!(kb0 == 0 && kb1 == Kb)) {
+      if (kClusterSplit && !(kb0 == 0 && kb1 == Kb)) {
+        // this CTA's partial stays in its own shared memory (the stage area
+        // is idle: every load has been consumed); reduced across the cluster
+        // below
+        float* part = reinterpret_cast<float*>(smW);
+#pragma unroll
+        for (int j = 0; j < MP; ++j)
+          if (j < M) part[j * 128 + t] = acc[j];
+        write = false;
+      } else if (!(kb0 == 0 && kb1 == Kb)) {
         // split tile: publish this CTA's partial; the last contributor reduces
         const int slot_idx = 2 * blockIdx.x + (tile == first_tile ? 0 : 1);
         float* mine = ws_partials + size_t(slot_idx) * MP * 128;
@@ -356,6 +378,44 @@ __global__ void __launch_bounds__(Cfg::kThreads, 2)
     }
   }
 
+  if (kClusterSplit && cluster > 1) {
+    // every CTA of the cluster has its partial in shared memory
+    __syncwarp();
+    cluster_sync();
+    if (warp < 4) {
+      // this CTA sums rows [r0, r1) of the tile over the partials of ranks
+      // 0..C-1 in rank order (= K order: deterministic)
+      const int t = threadIdx.x;
+      const int C = cluster;
+      const int M = args.M;
+      const int r0 = crank * M / C, r1 = (crank + 1) * M / C;
+      const int col = int(blockIdx.x) / C * 128 + t;
+      const float* part = reinterpret_cast<const float*>(smW);
+      const float* src[kMaxCluster];
+#pragma unroll
+      for (int r = 0; r < kMaxCluster; ++r) src[r] = map_shared_rank(part, uint32_t(r < C ? r : 0));
+      for (int j = r0; j < r1; j += 4) {
+        float v[4][kMaxCluster];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+          for (int r = 0; r < kMaxCluster; ++r)
+            v[q][r] = (r < C && j + q < r1) ? src[r][(j + q) * 128 + t] : 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float sum = v[q][0];
+#pragma unroll
+          for (int r = 1; r < kMaxCluster; ++r)
+            if (r < C) sum += v[q][r];
+          if (j + q < r1 && col < args.N)
+            args.D[size_t(j + q) * args.N + col] = __float2bfloat16_rn(sum);
+        }
+      }
+    }
+    __syncwarp();
+    cluster_sync();  // the partners are done reading this CTA's partial
+  }
+
   __syncthreads();
   if (warp == Cfg::kMmaWarp) {
     tc_fence_after();
@@ -363,43 +423,117 @@ __global__ void __launch_bounds__(Cfg::kThreads, 2)
   }
 }
 
+// Sets the kernels' launch attributes once per device.
 template <class Cfg>
-cudaError_t run(const LaunchCtx& c, const GemmArgs& a, void* ws, size_t ws_bytes) {
+cudaError_t prepare_kernels(int dev) {
+  static unsigned long long done = 0;  // one bit per device
+  if (done >> (dev & 63) & 1ull) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(gemm_small_m_kernel<Cfg, false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       int(Cfg::kSmemBytes));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gemm_small_m_kernel<Cfg, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, int(Cfg::kSmemBytes));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gemm_small_m_kernel<Cfg, true>,
+                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e == cudaSuccess) done |= 1ull << (dev & 63);
+  return e;
+}
+
+// Whether a cluster of C CTAs of the cluster kernel can be resident at all
+// (sizes above 8 are not guaranteed); cached per device and C.
+template <class Cfg>
+bool cluster_fits(int dev, int C) {
+  static signed char known[64][kMaxCluster + 1] = {};  // 0 unknown, 1 yes, -1 no
+  signed char& k = known[dev & 63][C];
+  if (k == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(C);
+    cfg.blockDim = dim3(Cfg::kThreads);
+    cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = C;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    const bool ok = prepare_kernels<Cfg>(dev) == cudaSuccess &&
+                    cudaOccupancyMaxActiveClusters(&n, gemm_small_m_kernel<Cfg, true>, &cfg) ==
+                        cudaSuccess &&
+                    n > 0;
+    if (!ok) cudaGetLastError();  // a refused query leaves no sticky error
+    k = ok ? 1 : -1;
+  }
+  return k > 0;
+}
+
+// Split factor C for the cluster form, 0 for stream-K.  First choice: the
+// largest portable C <= 8 that keeps tiles * C within two CTAs per SM;
+// otherwise (few tiles) the largest C <= 16 within one CTA per SM.  Either
+// is taken only when tiles * C fills at least 70 % of the SMs; below that,
+// and above two tiles per SM, stream-K balances better.
+template <class Cfg>
+int cluster_split(const LaunchCtx& c, int n_tiles, int Kb) {
+  const long long fill = 7LL * c.num_sms;  // x10: 70 %
+  int best = 0;
+  for (int cl = 1; cl <= 8 && cl <= Kb; ++cl)
+    if ((long long)n_tiles * cl <= 2LL * c.num_sms) best = cl;
+  if (best > 0 && (long long)n_tiles * best * 10 >= fill) return best;
+  best = 0;
+  for (int cl = 9; cl <= kMaxCluster && cl <= Kb; ++cl)
+    if ((long long)n_tiles * cl <= c.num_sms) best = cl;
+  if (best > 0 && (long long)n_tiles * best * 10 >= fill) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cluster_fits<Cfg>(dev, best)) return best;
+  }
+  return 0;
+}
+
+template <class Cfg>
+cudaError_t run(const LaunchCtx& c, const GemmArgs& a, void* ws, size_t ws_bytes,
+                bool allow_cluster) {
   const int Kb = a.K / kBlockK;
   const int n_tiles = ceil_div(a.N, 128);
   const long long U = (long long)n_tiles * Kb;
-  const int grid = int(U < c.num_sms ? U : c.num_sms);
+  const int split = allow_cluster ? cluster_split<Cfg>(c, n_tiles, Kb) : 0;
+  const int grid = split > 0 ? n_tiles * split : int(U < c.num_sms ? U : c.num_sms);
   if (grid == 0) return cudaSuccess;
-  if (size_t(n_tiles) * 4 > size_t(kCounterBytes) ||
-      ws_bytes < size_t(kCounterBytes) + size_t(2) * grid * Cfg::MP * 128 * 4)
+  if (split == 0 && (size_t(n_tiles) * 4 > size_t(kCounterBytes) ||
+                     ws_bytes < size_t(kCounterBytes) + size_t(2) * grid * Cfg::MP * 128 * 4))
     return cudaErrorInvalidValue;
   CUtensorMap tmW, tmX;
   if (!make_tmap_u8_sw128(&tmW, a.B, uint64_t(a.N), a.K, 128)) return cudaErrorInvalidValue;
   if (!make_tmap_u8_sw128(&tmX, a.A, uint64_t(a.M), a.K, Cfg::MP)) return cudaErrorInvalidValue;
-  auto kern = gemm_small_m_kernel<Cfg>;
-  static unsigned long long attr_done = 0;  // one bit per device
   int dev = 0;
   cudaGetDevice(&dev);
-  if (!(attr_done >> (dev & 63) & 1ull)) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(Cfg::kSmemBytes));
-    if (e != cudaSuccess) return e;
-    attr_done |= 1ull << (dev & 63);
-  }
-  int* counters = reinterpret_cast<int*>(ws);
-  float* partials = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kCounterBytes);
+  if (cudaError_t e = prepare_kernels<Cfg>(dev)) return e;
+  int* counters = split > 0 ? nullptr : reinterpret_cast<int*>(ws);
+  float* partials =
+      split > 0 ? nullptr : reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kCounterBytes);
   // launched as a programmatic dependent of the previous kernel in the stream
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(Cfg::kThreads);
   cfg.dynamicSmemBytes = Cfg::kSmemBytes;
   cfg.stream = c.stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = split > 0 ? split : 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tmW, tmX, a, partials, counters, c.status);
+  cfg.numAttrs = split > 0 ? 2 : 1;
+  if (split > 0)
+    return cudaLaunchKernelEx(&cfg, gemm_small_m_kernel<Cfg, true>, tmW, tmX, a, partials,
+                              counters, c.status, split);
+  return cudaLaunchKernelEx(&cfg, gemm_small_m_kernel<Cfg, false>, tmW, tmX, a, partials,
+                            counters, c.status, 1);
 }
 
 }  // namespace
@@ -410,9 +544,23 @@ size_t small_m_workspace_bytes(int num_sms, int /*N*/) {
 
 cudaError_t launch_gemm_small_m(const LaunchCtx& c, const GemmArgs& a, void* ws,
                                 size_t ws_bytes) {
-  if (a.M <= 16) return run<SmCfg<16>>(c, a, ws, ws_bytes);
-  if (a.M <= 32) return run<SmCfg<32>>(c, a, ws, ws_bytes);
-  return run<SmCfg<64>>(c, a, ws, ws_bytes);
+  if (a.M <= 16) return run<SmCfg<16>>(c, a, ws, ws_bytes, false);
+  if (a.M <= 32) return run<SmCfg<32>>(c, a, ws, ws_bytes, false);
+  return run<SmCfg<64>>(c, a, ws, ws_bytes, false);
+}
+
+bool small_m_uses_workspace(const LaunchCtx& c, const GemmArgs& a) {
+  const int n_tiles = ceil_div(a.N, 128), Kb = a.K / kBlockK;
+  if (a.M <= 16) return cluster_split<SmCfg<16>>(c, n_tiles, Kb) == 0;
+  if (a.M <= 32) return cluster_split<SmCfg<32>>(c, n_tiles, Kb) == 0;
+  return cluster_split<SmCfg<64>>(c, n_tiles, Kb) == 0;
+}
+
+cudaError_t launch_gemm_small_m_any(const LaunchCtx& c, const GemmArgs& a, void* ws,
+                                    size_t ws_bytes) {
+  if (a.M <= 16) return run<SmCfg<16>>(c, a, ws, ws_bytes, true);
+  if (a.M <= 32) return run<SmCfg<32>>(c, a, ws, ws_bytes, true);
+  return run<SmCfg<64>>(c, a, ws, ws_bytes, true);
 }
 
 }  // namespace fp8gemm

@@ -236,6 +236,16 @@ __device__ __forceinline__ void cluster_sync() {
                    : "memory");
 }
 
+// Generic address of the same shared-memory location in CTA `rank` of the
+// cluster (distributed shared memory); plain loads through it are ordered
+// by the cluster barrier like any other memory access.
+template <class T>
+__device__ __forceinline__ const T* map_shared_rank(const T* p, uint32_t rank) {
+  uint64_t r;
+  asm volatile("mapa.u64 %0, %1, %2;" : "=l"(r) : "l"(reinterpret_cast<uint64_t>(p)), "r"(rank));
+  return reinterpret_cast<const T*>(r);
+}
+
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }

@@ -33,6 +33,10 @@ def _run(A, sA, B, sB):
     (5, 264, 384, "normal"),        # small M, ragged N tile
     (33, 1000, 1280, "normal"),
     (17, 128, 16384, "decode"),     # split-K over one N tile
+    (3, 3840, 1280, "decode"),      # K split over an 8-CTA cluster, fewer rows than CTAs
+    (33, 2816, 768, "decode"),      # 6-CTA cluster, uneven row shares
+    (20, 1536, 7168, "decode"),     # 12-CTA cluster (above the portable size)
+    (2, 24576, 1536, "decode"),     # one whole tile per CTA, no split
 ])
 def test_dense_matches_oracle(M, N, K, kind):
     A, sA, B, sB = quantised_dense(M, N, K, kind, seed=M * 7 + N)
