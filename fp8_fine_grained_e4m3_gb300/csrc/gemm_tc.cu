@@ -14,7 +14,8 @@
 //
 // CTA layout (384 threads, one CTA per SM, persistent over tiles):
 //   warps 0-7  promotion + epilogue: two warpgroups; warpgroup g owns columns
-//              [g*BN/2, (g+1)*BN/2) of the tile, thread = tile row (TMEM lane)
+//              [g*BN/2, (g+1)*BN/2) of the tile, thread = tile row (TMEM lane),
+//              reading each K block's partial in 64-column TMEM loads
 //   warp 8     TMA producer: A tile 128x128 B and B tile BNx128 B per K block
 //              into a kStages-deep shared-memory ring (128-byte swizzle)
 //   warp 9     MMA issuer (one thread): 4 x tcgen05.mma kind::f8f6f4 (K = 32)
@@ -51,19 +52,26 @@ struct TcCfg {
   static constexpr int kMmaWarp = 9;
   static constexpr int kThreads = 384;  // 3 warpgroups; warps 10-11 only donate registers
   // Launch cap is 65536 / 384 -> 168 registers.  The producer warpgroup drops
-  // to kLowRegs and the two promotion warpgroups rise to kHighRegs:
-  // 4*32*104 + 8*32*200 = 64512 = 384*168.
-  static constexpr uint32_t kLowRegs = 104;
-  static constexpr uint32_t kHighRegs = 200;
+  // to kLowRegs and the two promotion warpgroups rise to kHighRegs (BN = 256:
+  // a 128-column accumulator plus a 64-column TMEM chunk per thread):
+  // 128*72 + 256*216 = 128*104 + 256*200 = 64512 = 384*168; per sub-partition
+  // (one producer and two promotion warps share its 512 registers per lane)
+  // low + 2*high <= 512.
+  static constexpr uint32_t kLowRegs = BN == 256 ? 72 : 104;
+  static constexpr uint32_t kHighRegs = BN == 256 ? 216 : 200;
+  static_assert(128 * kLowRegs + 256 * kHighRegs <= 384 * 168, "register split");
+  static_assert(kLowRegs + 2 * kHighRegs <= 512, "register split per sub-partition");
   static constexpr int kABytes = kBlockM * kBlockK;  // 16 KB
   static constexpr int kBBytes = BN * kBlockK;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kColsPerWG = BN / 2;
-  static constexpr int kTmemCols = 2 * BN;  // two partial buffers
+  static constexpr int kTmemBufs = 2;       // TMEM partial buffers
+  static constexpr int kTmemCols = kTmemBufs * BN;
   static constexpr int kBarBytes = 512;
   static constexpr size_t kSmemBytes = 1024 + size_t(kStages) * kStageBytes + kBarBytes;
   static_assert(BN == 128 || BN == 256, "BN");
   static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM columns must be a power of 2");
+  static_assert((2 * kStages + 2 * kTmemBufs + 1) * 8 + 8 <= kBarBytes, "barrier area");
 };
 
 struct Tile {
@@ -180,9 +188,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   uint64_t* full_bar = bars;
   uint64_t* empty_bar = bars + kStages;
   uint64_t* tfull_bar = bars + 2 * kStages;
-  uint64_t* tempty_bar = bars + 2 * kStages + 2;
-  uint64_t* drain_bar = bars + 2 * kStages + 4;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
+  constexpr int NB = Cfg::kTmemBufs;
+  uint64_t* tempty_bar = bars + 2 * kStages + NB;
+  uint64_t* drain_bar = bars + 2 * kStages + 2 * NB;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 2 * NB + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x / 32;
@@ -193,7 +202,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NB; ++b) {
       mbar_init(&tfull_bar[b], 1);
       mbar_init(&tempty_bar[b], Cfg::kPromoWarps);
     }
@@ -264,8 +273,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         for (int kb = 0; kb < Kb; ++kb, ++it) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1;
-          const int buf = it & 1;
-          const uint32_t tph = (it >> 1) & 1;
+          const int buf = it % NB;
+          const uint32_t tph = (it / NB) & 1;
           if (!mbar_wait(&tempty_bar[buf], tph ^ 1, abort_flag) ||
               !mbar_wait(&full_bar[s], ph, abort_flag)) {
             fail();
@@ -321,8 +330,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           sa_next = row_ok ? __ldg(sa_ptr + kb + 1) : 0.f;
           sb_next = cols_ok ? __ldg(sb_ptr + kb + 1) : 0.f;
         }
-        const int buf = it & 1;
-        const uint32_t tph = (it >> 1) & 1;
+        const int buf = it % NB;
+        const uint32_t tph = (it / NB) & 1;
         if (!mbar_wait(&tfull_bar[buf], tph, abort_flag)) {
           fail();
           ok = false;
@@ -331,34 +340,27 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         tc_fence_after();
         const uint32_t taddr = tmem_base + lane_base + buf * BN + wg * Cfg::kColsPerWG;
         const float2 sc2 = make_float2(sc, sc);
-        // 16-column chunks, double-buffered: the load of chunk c+1 is in
-        // flight while chunk c is scaled and added; the TMEM buffer goes back
-        // to the MMA warp as soon as the last chunk has landed in registers.
-        constexpr int kChunks = Cfg::kColsPerWG / 16;
-        uint32_t ra[16], rb[16];
-        auto release = [&]() {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&tempty_bar[buf]);
-        };
-        auto promote = [&](const uint32_t(&r)[16], int c) {
+        // 64-column chunks, one TMEM load each (BN = 256: two per K block).
+        // Few wide loads beat many narrow ones: a warp's loads complete one
+        // after another, so each costs its own latency.  The TMEM buffer goes
+        // back to the MMA warp as soon as the last chunk has landed.
+        constexpr int kChunks = Cfg::kColsPerWG / 64;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float2 p = make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-            acc[c * 8 + j] = __ffma2_rn(p, sc2, acc[c * 8 + j]);
+        for (int c = 0; c < kChunks; ++c) {
+          uint32_t r[64];
+          tmem_ld_32x32b_x64(taddr + c * 64, r);
+          tmem_ld_wait_tied(*reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+          reg_tie32(&r[32]);
+          if (c + 1 == kChunks) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty_bar[buf]);
           }
-        };
-        tmem_ld_32x32b_x16(taddr, ra);
-        tmem_ld_wait_tied16(ra);
 #pragma unroll
-        for (int c = 0; c < kChunks; c += 2) {
-          tmem_ld_32x32b_x16(taddr + (c + 1) * 16, rb);
-          promote(ra, c);
-          tmem_ld_wait_tied16(rb);
-          if (c + 2 == kChunks) release();
-          if (c + 2 < kChunks) tmem_ld_32x32b_x16(taddr + (c + 2) * 16, ra);
-          promote(rb, c + 1);
-          if (c + 2 < kChunks) tmem_ld_wait_tied16(ra);
+          for (int j = 0; j < 32; ++j) {
+            const float2 p = make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+            acc[c * 32 + j] = __ffma2_rn(p, sc2, acc[c * 32 + j]);
+          }
         }
       }
       if (!ok) break;
