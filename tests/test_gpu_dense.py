@@ -24,6 +24,8 @@ def _run(A, sA, B, sB):
     (256, 512, 640, "prefill"),     # 256-wide N tiles, outlier columns
     (65, 256, 256, "normal"),       # smallest M on the large-M path
     (520, 2304, 384, "prefill"),    # many tiles, 256-wide N tiles, ragged M
+    (257, 768, 1024, "prefill"),    # one row into a third M tile
+    (777, 2176, 512, "normal"),     # N >= 2048 not a multiple of 256: half-empty last N tile
     (1, 7168, 2048, "decode"),      # decode shapes, whole
     (16, 7168, 2048, "decode"),
     (64, 7168, 2048, "decode"),
