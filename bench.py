@@ -378,7 +378,17 @@ def measure_configs(peaks, dev):
             r = _roof(2 * M * N * K, gemm_bytes(M, N, K), ms, peaks)
             r["timing"] = "CUDA graph, 24 rotating weight copies"
             res[f"decode_{M}x{N}x{K}"] = r
-            del copies, fns
+            # From FP32 activations: fp8gemm_dense_quant_a (the quantiser, then
+            # the GEMM as its programmatic dependent)
+            X, _ = synthetic.dense_operands_device(M, 8, K, kind="decode", seed=M, device=dev)
+            fns_q = [(lambda Bc=Bc, sBc=sBc: b.fp8gemm_dense_quant_a(X, Bc, sBc, D=D))
+                     for Bc, sBc in copies]
+            nb = gemm_bytes(M, N, K) - M * K - 4 * M * (K // 128) + 4 * M * K
+            ms_q = time_graph(fns_q, reps=4)
+            r = _roof(2 * M * N * K, nb, ms_q, peaks)
+            r["timing"] = "CUDA graph, 24 rotating weight copies; quantiser + GEMM, 2 launches"
+            res[f"decode_quant_a_{M}x{N}x{K}"] = r
+            del copies, fns, fns_q, X
 
     # quantiser on the large prefill activations
     X, _ = synthetic.dense_operands_device(4096, 8, 16384, kind="prefill", seed=0, device=dev)

@@ -37,6 +37,7 @@ SIGNATURES = [
     ("fp8_quant_1x128", _I, [_P, _P, _P, _I, _I, _P]),
     ("fp8_quant_128x128", _I, [_P, _P, _P, _I, _I, _I, _P]),
     ("fp8gemm_dense", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _P]),
+    ("fp8gemm_dense_quant_a", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
     ("fp8gemm_grouped_contiguous", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     ("fp8gemm_grouped_masked", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     ("fp8gemm_dense_small_m_noalloc", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _P]),
@@ -179,6 +180,26 @@ def fp8gemm_dense(A, sA, B, sB, D=None, stream=None):
         D = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
     _check(lib().fp8gemm_dense(_ptr(A), _ptr(_f32(sA, "sA")), _ptr(B), _ptr(_f32(sB, "sB")),
                                _ptr(_dev(D, "D")), M, N, K, _stream(stream)), "fp8gemm_dense")
+    return D
+
+
+def fp8gemm_dense_quant_a(X, B, sB, D=None, Q=None, sA=None, stream=None):
+    """X f32 [M, K], B u8 [N, K], sB [ceil(N/128), K/128] -> D bf16 [M, N], with A
+    quantised 1x128 on load.  Q u8 [M, K] and sA f32 [M, K/128] (both or neither)
+    receive the quantised activations."""
+    torch = _torch()
+    X, B = _f32(X, "X"), _u8(B, "B")
+    M, K = X.shape
+    N = B.shape[0]
+    if D is None:
+        D = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    if (Q is None) != (sA is None):
+        raise ValueError("Q and sA go together: give both or neither")
+    qp = _ptr(_u8(Q, "Q")) if Q is not None else None
+    sp = _ptr(_f32(sA, "sA")) if sA is not None else None
+    _check(lib().fp8gemm_dense_quant_a(_ptr(X), qp, sp, _ptr(B), _ptr(_f32(sB, "sB")),
+                                       _ptr(_dev(D, "D")), M, N, K, _stream(stream)),
+           "fp8gemm_dense_quant_a")
     return D
 
 

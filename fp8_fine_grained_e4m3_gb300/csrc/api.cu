@@ -7,6 +7,7 @@
 #include <atomic>
 #include <map>
 #include <mutex>
+#include <tuple>
 #include <utility>
 
 #include "common.cuh"
@@ -29,7 +30,7 @@ struct DeviceInfo {
 
 std::mutex g_mu;
 std::map<int, DeviceInfo> g_devices;
-std::map<std::pair<int, cudaStream_t>, std::pair<void*, size_t>> g_workspaces;
+std::map<std::tuple<int, cudaStream_t, int>, std::pair<void*, size_t>> g_workspaces;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -85,13 +86,18 @@ int finish(cudaError_t e, int nlaunch) {
   return FP8GEMM_OK;
 }
 
-// Workspace for the split-K reduction of the small-M path, one per
-// (device, stream), zero-initialised (its counters must start at 0).
-int workspace_for(cudaStream_t s, size_t bytes, void** out) {
+// Library-owned device buffers, one per (device, stream, slot), zero-
+// initialised.  Slot kWsSplitK: the split-K reduction of the small-M path (its
+// counters must start at 0 and are left at 0).  Slot kWsQuantA: quantised
+// activations of fp8gemm_dense_quant_a at large M -- a separate buffer, so
+// those bytes never land on the counters.
+enum { kWsSplitK = 0, kWsQuantA = 1 };
+
+int workspace_for(cudaStream_t s, size_t bytes, void** out, int slot = kWsSplitK) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FP8GEMM_ERR_LAUNCH;
   std::lock_guard<std::mutex> lk(g_mu);
-  auto key = std::make_pair(dev, s);
+  auto key = std::make_tuple(dev, s, slot);
   auto it = g_workspaces.find(key);
   if (it != g_workspaces.end() && it->second.second >= bytes) {
     *out = it->second.first;
@@ -207,6 +213,30 @@ int fp8gemm_dense(const uint8_t* A, const float* sA, const uint8_t* B, const flo
     return finish(launch_gemm_small_m_any(c, a, ws, bytes), 1);
   }
   return finish(launch_gemm_tc(c, a), 1);
+}
+
+int fp8gemm_dense_quant_a(const float* X, uint8_t* Q, float* sA, const uint8_t* B,
+                          const float* sB, void* D, int M, int N, int K,
+                          fp8gemm_stream_t stream) {
+  if (int r = check_common(M, N, K)) return r;
+  if (M == 0 || N == 0) return FP8GEMM_OK;
+  if (!X || !B || !sB || !D || (Q == nullptr) != (sA == nullptr)) return FP8GEMM_ERR_NULL;
+  if (!aligned16(X) || !aligned16(B) || !aligned16(sB) || !aligned16(D) ||
+      (Q && (!aligned16(Q) || !aligned16(sA))))
+    return FP8GEMM_ERR_ALIGN;
+  if ((long long)M * K > (1LL << 46)) return FP8GEMM_ERR_SHAPE;
+  if (!Q) {  // quantised A in the library's buffer: bytes, then (16-B aligned) scales
+    const size_t qbytes = (size_t(M) * K + 15) / 16 * 16;
+    void* ws = nullptr;
+    if (int r = workspace_for(stream, qbytes + size_t(M) * (K / kBlockK) * 4, &ws, kWsQuantA))
+      return r;
+    Q = static_cast<uint8_t*>(ws);
+    sA = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + qbytes);
+  }
+  // the quantiser, then the GEMM as its programmatic dependent: the GEMM's
+  // prologue and weight prefetch overlap the quantiser
+  if (int r = fp8_quant_1x128(X, Q, sA, M, K, stream)) return r;
+  return fp8gemm_dense(Q, sA, B, sB, D, M, N, K, stream);
 }
 
 int fp8gemm_grouped_contiguous(const uint8_t* A, const float* sA, const uint8_t* B,

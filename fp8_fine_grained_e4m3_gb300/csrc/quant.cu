@@ -12,6 +12,7 @@
 // per element): loads are 16-byte vectors and every warp writes whole 128-byte
 // output rows.
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace fp8gemm {
 namespace {
@@ -38,7 +39,10 @@ constexpr int kQuantUnroll = 4;  // 1x128 blocks per warp (loads kept in flight)
 
 // One warp per group of kQuantUnroll consecutive 1x128 blocks.  Block b
 // covers elements [128 b, 128 b + 128) of the row-major [M, K] input (K is a
-// multiple of 128), and its scale is sX[b].
+// multiple of 128), and its scale is sX[b].  kPdl: launched as a
+// programmatic dependent of the previous kernel (wait for it before the first
+// load; let the next kernel launch right away).
+template <bool kPdl>
 __global__ void __launch_bounds__(256) quant_1x128_kernel(const float4* __restrict__ X,
                                                           uint32_t* __restrict__ Q,
                                                           float* __restrict__ sX,
@@ -46,6 +50,10 @@ __global__ void __launch_bounds__(256) quant_1x128_kernel(const float4* __restri
   const long long warp0 =
       ((long long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32) * kQuantUnroll;
   const int lane = threadIdx.x % 32;
+  if constexpr (kPdl) {
+    griddep_wait();
+    griddep_launch_dependents();
+  }
   float4 v[kQuantUnroll];
 #pragma unroll
   for (int u = 0; u < kQuantUnroll; ++u) {
@@ -121,9 +129,26 @@ cudaError_t launch_quant_1x128(const LaunchCtx& c, const float* X, uint8_t* Q, f
   const long long per_cta = 8LL * kQuantUnroll;
   const long long grid = (nblocks + per_cta - 1) / per_cta;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
-  quant_1x128_kernel<<<unsigned(grid), 256, 0, c.stream>>>(
-      reinterpret_cast<const float4*>(X), reinterpret_cast<uint32_t*>(Q), sX, nblocks);
-  return cudaGetLastError();
+  if (grid > 8LL * c.num_sms) {  // more than one wave: plain launch
+    quant_1x128_kernel<false><<<unsigned(grid), 256, 0, c.stream>>>(
+        reinterpret_cast<const float4*>(X), reinterpret_cast<uint32_t*>(Q), sX, nblocks);
+    return cudaGetLastError();
+  }
+  // A decode-sized quantisation (one wave) is launched as a programmatic
+  // dependent of the previous kernel, so that its launch, and the prologue of
+  // the GEMM after it, overlap the kernel before.  (Not for large grids: there
+  // every short CTA would pay the dependency wait.)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(grid));
+  cfg.blockDim = dim3(256);
+  cfg.stream = c.stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, quant_1x128_kernel<true>, reinterpret_cast<const float4*>(X),
+                            reinterpret_cast<uint32_t*>(Q), sX, nblocks);
 }
 
 cudaError_t launch_quant_128x128(const LaunchCtx& c, const float* W, uint8_t* Q, float* sW,

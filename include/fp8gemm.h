@@ -107,6 +107,30 @@ int fp8gemm_dense(const uint8_t* A, const float* sA, const uint8_t* B, const flo
                   void* D, int M, int N, int K, fp8gemm_stream_t stream);
 
 /*
+ * fp8gemm_dense_quant_a -- fp8gemm_dense on FP32 activations: A and sA are
+ * the 1x128 quantisation of X (fp8_quant_1x128's rule, same bytes and
+ * scales), produced on the way into the GEMM ("news.rkmt.cn/news/5092"
+ * section 2.3 and "bhfrc.com/news/60211" section 6: the scale work belongs
+ * with the producer, not in a separate step of the caller).
+ *
+ *   X  f32 [M, K]  (input)
+ *   Q  u8 [M, K], sA f32 [M, K/128] (optional outputs: both NULL, or both
+ *      given to receive the quantised activations, e.g. to reuse them)
+ *   B  u8 [N, K]   sB f32 [ceil(N/128), K/128]
+ *   D  bf16 [M, N] (output, written in full)
+ *   M >= 0, N % 8 == 0, K % 128 == 0, K > 0; all pointers 16-B aligned.
+ *
+ * Two kernels on `stream`: the quantiser, then the GEMM launched as its
+ * programmatic dependent, so the GEMM's launch, prologue and weight prefetch
+ * overlap the quantiser.  With Q/sA NULL the quantised A lives in a
+ * library-owned per-stream buffer of about M*K*(1 + 4/128) bytes.  Exactly
+ * one of Q, sA NULL returns FP8GEMM_ERR_NULL.
+ */
+int fp8gemm_dense_quant_a(const float* X, uint8_t* Q, float* sA, const uint8_t* B,
+                          const float* sB, void* D, int M, int N, int K,
+                          fp8gemm_stream_t stream);
+
+/*
  * fp8gemm_grouped_contiguous -- MoE experts in one launch, each expert's
  * tokens a contiguous row segment of A ("news.rkmt.cn/news/5092" section 5.3;
  * "news.rkmt.cn/news/5092" section 1.2: one launch for many experts).

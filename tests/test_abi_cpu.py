@@ -29,7 +29,7 @@ def lib():
 
 def test_header_declares_the_boundary():
     names = set(_declared_functions())
-    for n in ["fp8_quant_1x128", "fp8_quant_128x128", "fp8gemm_dense",
+    for n in ["fp8_quant_1x128", "fp8_quant_128x128", "fp8gemm_dense", "fp8gemm_dense_quant_a",
               "fp8gemm_grouped_contiguous", "fp8gemm_grouped_masked",
               "fp8gemm_get_device_status", "fp8gemm_strerror"]:
         assert n in names
@@ -66,6 +66,12 @@ def test_host_validation_needs_no_gpu(lib):
                                           100, 256, 256, 2, s) == b.ERR_SHAPE
     assert lib.fp8gemm_grouped_masked(good, good, good, good, good, good,
                                       0, 128, 256, 256, s) == b.OK
+    assert lib.fp8gemm_dense_quant_a(good, None, None, good, good, good, 4, 256, 200, s) == b.ERR_SHAPE
+    assert lib.fp8gemm_dense_quant_a(good, good, None, good, good, good, 4, 256, 256, s) == b.ERR_NULL
+    assert lib.fp8gemm_dense_quant_a(None, None, None, good, good, good, 4, 256, 256, s) == b.ERR_NULL
+    assert lib.fp8gemm_dense_quant_a(P((1 << 20) + 8), None, None, good, good, good,
+                                     4, 256, 256, s) == b.ERR_ALIGN
+    assert lib.fp8gemm_dense_quant_a(good, None, None, good, good, good, 0, 256, 256, s) == b.OK
     assert lib.fp8_quant_1x128(good, good, good, 4, 130, s) == b.ERR_SHAPE
     assert lib.fp8_quant_128x128(good, None, good, 1, 8, 128, s) == b.ERR_NULL
     assert lib.fp8gemm_get_device_status(s, None) == b.ERR_NULL
