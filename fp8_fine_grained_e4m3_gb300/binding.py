@@ -138,8 +138,8 @@ def _ptr(t):
 
 # ------------------------------------------------------------ entry points
 def fp8_quant_1x128(X, Q=None, sX=None, stream=None):
-    """X f32 [..., K] -> (Q u8 [..., K], sX f32 [..., K/128]).  Leading dims are
-    flattened into M."""
+    """X f32 [..., K] -> (Q u8 [..., K], sX f32 [..., ceil(K/128)]).  Leading dims
+    are flattened into M."""
     torch = _torch()
     X = _f32(X, "X")
     K = X.shape[-1]
@@ -147,7 +147,7 @@ def fp8_quant_1x128(X, Q=None, sX=None, stream=None):
     if Q is None:
         Q = torch.empty(X.shape, dtype=torch.uint8, device=X.device)
     if sX is None:
-        sX = torch.empty((*X.shape[:-1], max(K // 128, 0)), dtype=torch.float32, device=X.device)
+        sX = torch.empty((*X.shape[:-1], -(-K // 128)), dtype=torch.float32, device=X.device)
     _check(lib().fp8_quant_1x128(_ptr(X), _ptr(_u8(Q, "Q")), _ptr(_f32(sX, "sX")), M, K,
                                  _stream(stream)), "fp8_quant_1x128")
     return Q, sX
@@ -163,7 +163,7 @@ def fp8_quant_128x128(W, Q=None, sW=None, stream=None):
     if Q is None:
         Q = torch.empty(W.shape, dtype=torch.uint8, device=W.device)
     if sW is None:
-        shp = ((N + 127) // 128, K // 128)
+        shp = ((N + 127) // 128, -(-K // 128))
         sW = torch.empty(shp if squeeze else (E, *shp), dtype=torch.float32, device=W.device)
     _check(lib().fp8_quant_128x128(_ptr(W3), _ptr(_u8(Q, "Q")), _ptr(_f32(sW, "sW")), E, N, K,
                                    _stream(stream)), "fp8_quant_128x128")

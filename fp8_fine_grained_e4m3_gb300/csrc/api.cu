@@ -143,12 +143,15 @@ using namespace fp8gemm;
 
 namespace {
 
-// Shared shape rules: K a positive multiple of 128, N a multiple of 8, sizes
-// non-negative, and every byte offset the kernels form within int64 / int32
-// index range.
+// K granularity: a TMA row stride (K bytes of e4m3) must be a multiple of 16
+// bytes.  K need not be a multiple of 128: the last K block is then partial
+// and the copies fill its missing columns with zeros.
+constexpr int kKAlign = 16;
+
+// Shared shape rules: K a positive multiple of 16, sizes non-negative.
 int check_common(int M, int N, int K) {
   if (M < 0 || N < 0 || K < 0) return FP8GEMM_ERR_SHAPE;
-  if (K == 0 || K % kBlockK != 0 || N % 8 != 0) return FP8GEMM_ERR_SHAPE;
+  if (K == 0 || K % kKAlign != 0) return FP8GEMM_ERR_SHAPE;
   return FP8GEMM_OK;
 }
 
@@ -173,7 +176,7 @@ extern "C" {
 
 int fp8_quant_1x128(const float* X, uint8_t* Q, float* sX, int M, int K,
                     fp8gemm_stream_t stream) {
-  if (M < 0 || K < 0 || K % kBlockK != 0) return FP8GEMM_ERR_SHAPE;
+  if (M < 0 || K < 0 || K % kKAlign != 0) return FP8GEMM_ERR_SHAPE;
   if (M == 0 || K == 0) return FP8GEMM_OK;
   if (!X || !Q || !sX) return FP8GEMM_ERR_NULL;
   if (!aligned16(X) || !aligned16(Q) || !aligned16(sX)) return FP8GEMM_ERR_ALIGN;
@@ -184,7 +187,7 @@ int fp8_quant_1x128(const float* X, uint8_t* Q, float* sX, int M, int K,
 
 int fp8_quant_128x128(const float* W, uint8_t* Q, float* sW, int E, int N, int K,
                       fp8gemm_stream_t stream) {
-  if (E < 0 || N < 0 || K < 0 || K % kBlockK != 0) return FP8GEMM_ERR_SHAPE;
+  if (E < 0 || N < 0 || K < 0 || K % kKAlign != 0) return FP8GEMM_ERR_SHAPE;
   if (E == 0 || N == 0 || K == 0) return FP8GEMM_OK;
   if ((long long)E * N * (long long)K > (1LL << 46)) return FP8GEMM_ERR_SHAPE;
   if (!W || !Q || !sW) return FP8GEMM_ERR_NULL;
@@ -228,7 +231,8 @@ int fp8gemm_dense_quant_a(const float* X, uint8_t* Q, float* sA, const uint8_t* 
   if (!Q) {  // quantised A in the library's buffer: bytes, then (16-B aligned) scales
     const size_t qbytes = (size_t(M) * K + 15) / 16 * 16;
     void* ws = nullptr;
-    if (int r = workspace_for(stream, qbytes + size_t(M) * (K / kBlockK) * 4, &ws, kWsQuantA))
+    if (int r = workspace_for(stream, qbytes + size_t(M) * ceil_div(K, kBlockK) * 4, &ws,
+                              kWsQuantA))
       return r;
     Q = static_cast<uint8_t*>(ws);
     sA = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + qbytes);
@@ -296,7 +300,7 @@ const char* fp8gemm_strerror(int code) {
     case FP8GEMM_OK: return "ok";
     case FP8GEMM_ERR_NULL: return "a required pointer is NULL";
     case FP8GEMM_ERR_ALIGN: return "a pointer is not 16-byte aligned";
-    case FP8GEMM_ERR_SHAPE: return "unsupported shape (K % 128, N % 8, M_pad % 128, sign or range)";
+    case FP8GEMM_ERR_SHAPE: return "unsupported shape (K % 16, M_pad % 128, sign or range)";
     case FP8GEMM_ERR_ARCH: return "current device is not compute capability 10.3 (sm_103a)";
     case FP8GEMM_ERR_LAUNCH: return "CUDA launch or runtime call failed";
     case FP8GEMM_ERR_DEVICE_STATUS: return "device-side input error (expert index or row count)";

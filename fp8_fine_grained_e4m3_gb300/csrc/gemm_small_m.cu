@@ -110,7 +110,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 2)
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  const int Kb = args.K / kBlockK;
+  const int Kb = ceil_div(args.K, kBlockK);  // the last K block may be partial
   const int n_tiles = ceil_div(args.N, 128);
   const StreamK sk{(long long)n_tiles * Kb, int(gridDim.x), Kb};
   // units [u_begin, u_end): the stream-K range, or this CTA's part of its
@@ -496,7 +496,7 @@ int cluster_split(const LaunchCtx& c, int n_tiles, int Kb) {
 template <class Cfg>
 cudaError_t run(const LaunchCtx& c, const GemmArgs& a, void* ws, size_t ws_bytes,
                 bool allow_cluster) {
-  const int Kb = a.K / kBlockK;
+  const int Kb = ceil_div(a.K, kBlockK);
   const int n_tiles = ceil_div(a.N, 128);
   const long long U = (long long)n_tiles * Kb;
   const int split = allow_cluster ? cluster_split<Cfg>(c, n_tiles, Kb) : 0;
@@ -550,7 +550,7 @@ cudaError_t launch_gemm_small_m(const LaunchCtx& c, const GemmArgs& a, void* ws,
 }
 
 bool small_m_uses_workspace(const LaunchCtx& c, const GemmArgs& a) {
-  const int n_tiles = ceil_div(a.N, 128), Kb = a.K / kBlockK;
+  const int n_tiles = ceil_div(a.N, 128), Kb = ceil_div(a.K, kBlockK);
   if (a.M <= 16) return cluster_split<SmCfg<16>>(c, n_tiles, Kb) == 0;
   if (a.M <= 32) return cluster_split<SmCfg<32>>(c, n_tiles, Kb) == 0;
   return cluster_split<SmCfg<64>>(c, n_tiles, Kb) == 0;

@@ -101,7 +101,7 @@ struct Scheduler {
 
   __device__ void init(int BN, int* st) {
     status = st;
-    Kb = a.K / kBlockK;
+    Kb = ceil_div(a.K, kBlockK);  // the last K block may be partial (TMA fills zeros)
     num_n = ceil_div(a.N, BN);
     if (a.mode == GemmMode::kMasked) {
       num_m = ceil_div(a.M, kBlockM);
@@ -364,8 +364,17 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         }
       }
       if (!ok) break;
-      // epilogue: BF16 (round to nearest even), 16-byte stores
-      if (row_ok) {
+      // epilogue: BF16 (round to nearest even), 16-byte stores; rows of D
+      // are 16-byte aligned only when N % 8 == 0, else element stores
+      if (row_ok && args.N % 8 != 0) {
+        __nv_bfloat16* drow = args.D + size_t(tile.row0 + row) * args.N + col0;
+#pragma unroll
+        for (int j = 0; j < Cfg::kColsPerWG / 2; ++j) {
+          const __nv_bfloat162 p = __float22bfloat162_rn(acc[j]);
+          if (col0 + 2 * j < args.N) drow[2 * j] = p.x;
+          if (col0 + 2 * j + 1 < args.N) drow[2 * j + 1] = p.y;
+        }
+      } else if (row_ok) {
         __nv_bfloat16* drow = args.D + size_t(tile.row0 + row) * args.N + col0;
 #pragma unroll
         for (int j = 0; j < Cfg::kColsPerWG; j += 8) {

@@ -72,7 +72,7 @@ extern "C" int fp8gemm_dense_small_m_noalloc(const uint8_t* A, const float* sA, 
                                              const float* sB, void* D, int M, int N, int K,
                                              fp8gemm_stream_t stream) {
   if (M < 0 || N < 0 || K < 0) return FP8GEMM_ERR_SHAPE;
-  if (K == 0 || K % kBlockK != 0 || N % 8 != 0) return FP8GEMM_ERR_SHAPE;
+  if (K == 0 || K % 16 != 0) return FP8GEMM_ERR_SHAPE;  // TMA: row strides are 16-B multiples
   if (M == 0 || N == 0) return FP8GEMM_OK;
   const int n_tiles = ceil_div(N, 128);
   if (M > kNoAllocMaxM || size_t(n_tiles) * sizeof(int) > kNoAllocCounterBytes)

@@ -37,16 +37,18 @@ __device__ __forceinline__ float absmax4(float4 v) {
 
 constexpr int kQuantUnroll = 4;  // 1x128 blocks per warp (loads kept in flight)
 
-// One warp per group of kQuantUnroll consecutive 1x128 blocks.  Block b
-// covers elements [128 b, 128 b + 128) of the row-major [M, K] input (K is a
-// multiple of 128), and its scale is sX[b].  kPdl: launched as a
-// programmatic dependent of the previous kernel (wait for it before the first
-// load; let the next kernel launch right away).
-template <bool kPdl>
-__global__ void __launch_bounds__(256) quant_1x128_kernel(const float4* __restrict__ X,
+// One warp per group of kQuantUnroll consecutive 1x128 blocks; block b is
+// (row b / Kb, K block b % Kb) of the row-major [M, K] input and its scale is
+// sX[b].  When K is a multiple of 128 (kRagged false) block b is simply
+// elements [128 b, 128 b + 128); otherwise a row's last block holds the
+// K % 128 remaining elements (a multiple of 16) and its amax runs over those.
+// kPdl: launched as a programmatic dependent of the previous kernel (wait for
+// it before the first load; let the next kernel launch right away).
+template <bool kPdl, bool kRagged>
+__global__ void __launch_bounds__(256) quant_1x128_kernel(const float* __restrict__ X,
                                                           uint32_t* __restrict__ Q,
                                                           float* __restrict__ sX,
-                                                          long long nblocks) {
+                                                          long long nblocks, int K, int Kb) {
   const long long warp0 =
       ((long long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32) * kQuantUnroll;
   const int lane = threadIdx.x % 32;
@@ -55,10 +57,22 @@ __global__ void __launch_bounds__(256) quant_1x128_kernel(const float4* __restri
     griddep_launch_dependents();
   }
   float4 v[kQuantUnroll];
+  long long e0[kQuantUnroll];  // first element of the block
+  bool in[kQuantUnroll];       // this lane's 4 elements exist
 #pragma unroll
   for (int u = 0; u < kQuantUnroll; ++u) {
     const long long b = warp0 + u;
-    v[u] = b < nblocks ? __ldcs(X + b * 32 + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+    if constexpr (kRagged) {
+      const long long m = b / Kb;
+      const int kb = int(b - m * Kb);
+      e0[u] = m * K + kb * kBlockK;
+      in[u] = b < nblocks && lane * 4 < K - kb * kBlockK;
+    } else {
+      e0[u] = b * kBlockK;
+      in[u] = b < nblocks;
+    }
+    v[u] = in[u] ? __ldcs(reinterpret_cast<const float4*>(X + e0[u]) + lane)
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
   }
 #pragma unroll
   for (int u = 0; u < kQuantUnroll; ++u) {
@@ -68,18 +82,19 @@ __global__ void __launch_bounds__(256) quant_1x128_kernel(const float4* __restri
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     const float s = __fdiv_rn(amax, kE4M3Max);
-    Q[b * 32 + lane] = amax != 0.f ? quant4(v[u], s) : 0u;
+    if (in[u]) Q[e0[u] / 4 + lane] = amax != 0.f ? quant4(v[u], s) : 0u;
     if (lane == 0) sX[b] = s;
   }
 }
 
 // One CTA (256 threads) per 128x128 tile of one [N, K] matrix of the batch.
 // Thread t covers column group t % 32 (4 columns) of rows t / 32 + 8 i.
+// The last K tile may be partial (K % 128 columns, a multiple of 16).
 __global__ void __launch_bounds__(256) quant_128x128_kernel(const float* __restrict__ W,
                                                             uint8_t* __restrict__ Q,
                                                             float* __restrict__ sW, int N,
                                                             int K) {
-  const int Kb = K / kBlockK;
+  const int Kb = ceil_div(K, kBlockK);
   const int Nb = ceil_div(N, 128);
   const int kb = blockIdx.x;
   const int nb = blockIdx.y;
@@ -87,6 +102,7 @@ __global__ void __launch_bounds__(256) quant_128x128_kernel(const float* __restr
   const int cg = threadIdx.x % 32;
   const int r0 = threadIdx.x / 32;
   const size_t mat = size_t(e) * N * K;
+  const bool col_in = cg * 4 < K - kb * kBlockK;  // this thread's 4 columns exist
   __shared__ float red[8];
 
   float4 v[16];
@@ -94,7 +110,7 @@ __global__ void __launch_bounds__(256) quant_128x128_kernel(const float* __restr
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const int n = nb * 128 + r0 + 8 * i;
-    if (n < N) {
+    if (n < N && col_in) {
       v[i] = __ldcs(reinterpret_cast<const float4*>(W + mat + size_t(n) * K + kb * kBlockK) + cg);
       amax = fmaxf(amax, absmax4(v[i]));
     } else {
@@ -112,7 +128,7 @@ __global__ void __launch_bounds__(256) quant_128x128_kernel(const float* __restr
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const int n = nb * 128 + r0 + 8 * i;
-    if (n < N) {
+    if (n < N && col_in) {
       uint32_t* dst = reinterpret_cast<uint32_t*>(Q + mat + size_t(n) * K + kb * kBlockK) + cg;
       *dst = amax != 0.f ? quant4(v[i], s) : 0u;
     }
@@ -124,14 +140,21 @@ __global__ void __launch_bounds__(256) quant_128x128_kernel(const float* __restr
 
 cudaError_t launch_quant_1x128(const LaunchCtx& c, const float* X, uint8_t* Q, float* sX,
                                int M, int K) {
-  const long long nblocks = (long long)M * (K / kBlockK);
+  const int Kb = ceil_div(K, kBlockK);
+  const long long nblocks = (long long)M * Kb;
   if (nblocks == 0) return cudaSuccess;
   const long long per_cta = 8LL * kQuantUnroll;
   const long long grid = (nblocks + per_cta - 1) / per_cta;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const bool ragged = K % kBlockK != 0;
+  uint32_t* Q4 = reinterpret_cast<uint32_t*>(Q);
   if (grid > 8LL * c.num_sms) {  // more than one wave: plain launch
-    quant_1x128_kernel<false><<<unsigned(grid), 256, 0, c.stream>>>(
-        reinterpret_cast<const float4*>(X), reinterpret_cast<uint32_t*>(Q), sX, nblocks);
+    if (ragged)
+      quant_1x128_kernel<false, true><<<unsigned(grid), 256, 0, c.stream>>>(X, Q4, sX, nblocks,
+                                                                             K, Kb);
+    else
+      quant_1x128_kernel<false, false><<<unsigned(grid), 256, 0, c.stream>>>(X, Q4, sX, nblocks,
+                                                                              K, Kb);
     return cudaGetLastError();
   }
   // A decode-sized quantisation (one wave) is launched as a programmatic
@@ -147,8 +170,9 @@ cudaError_t launch_quant_1x128(const LaunchCtx& c, const float* X, uint8_t* Q, f
   attr.val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, quant_1x128_kernel<true>, reinterpret_cast<const float4*>(X),
-                            reinterpret_cast<uint32_t*>(Q), sX, nblocks);
+  if (ragged)
+    return cudaLaunchKernelEx(&cfg, quant_1x128_kernel<true, true>, X, Q4, sX, nblocks, K, Kb);
+  return cudaLaunchKernelEx(&cfg, quant_1x128_kernel<true, false>, X, Q4, sX, nblocks, K, Kb);
 }
 
 cudaError_t launch_quant_128x128(const LaunchCtx& c, const float* W, uint8_t* Q, float* sW,
@@ -156,7 +180,7 @@ cudaError_t launch_quant_128x128(const LaunchCtx& c, const float* W, uint8_t* Q,
   if (E == 0 || N == 0 || K == 0) return cudaSuccess;
   const int Nb = ceil_div(N, 128);
   if (Nb > 65535 || E > 65535) return cudaErrorInvalidValue;
-  dim3 grid(K / kBlockK, Nb, E);
+  dim3 grid(ceil_div(K, kBlockK), Nb, E);
   quant_128x128_kernel<<<grid, 256, 0, c.stream>>>(W, Q, sW, N, K);
   return cudaGetLastError();
 }

@@ -3,7 +3,7 @@
  * (1x128 / 128x128) FP32 scales and BF16 output, for GB300 (sm_103a).
  *
  * What is computed.  With A e4m3 [M, K] scaled per 1x128 tile (sA [M, Kb]) and
- * B e4m3 [N, K] scaled per 128x128 tile (sB [Nb, Kb]), Kb = K/128,
+ * B e4m3 [N, K] scaled per 128x128 tile (sB [Nb, Kb]), Kb = ceil(K/128),
  * Nb = ceil(N/128):
  *
  *   D[m, n] = bf16( sum_kb sA[m, kb] * sB[n/128, kb]
@@ -16,6 +16,13 @@
  * scaling core design" and "two-level accumulation").  The scale product
  * sA*sB is formed in FP32 and must be finite.
  *
+ * Shapes.  K is any positive multiple of 16 (a tensor copy's row stride must
+ * be a multiple of 16 bytes); when K is not a multiple of 128 the last K
+ * block holds the K % 128 remaining columns -- its scales cover those only,
+ * and the GEMM pads the block with zeros.  M and N are any non-negative
+ * sizes (the contiguous form keeps M_pad % 128 == 0).  Below, "K/128" in a
+ * scale shape means ceil(K/128).
+ *
  * Conventions shared by every call:
  *  - Every pointer is a DEVICE pointer owned by the caller; the library keeps
  *    no reference after the call returns.  Matrices are row-major with K
@@ -25,7 +32,7 @@
  *  - Host-side validation failures return a negative code and enqueue nothing:
  *    FP8GEMM_ERR_NULL (a required pointer is NULL), FP8GEMM_ERR_ALIGN (a base
  *    pointer is not 16-byte aligned), FP8GEMM_ERR_SHAPE (negative size,
- *    K % 128 != 0, N % 8 != 0, M_pad % 128 != 0, or a size past INT32 index
+ *    K % 16 != 0, K = 0, M_pad % 128 != 0, or a size past INT32 index
  *    range), FP8GEMM_ERR_ARCH (the current device is not compute capability
  *    10.3), FP8GEMM_ERR_LAUNCH (the CUDA launch itself failed).
  *  - Zero-sized problems (M = 0, M_pad = 0, E = 0, or N = 0) succeed and do
@@ -78,7 +85,7 @@ enum fp8gemm_status {
  * outside the contract.
  *
  *   X   f32 [M, K]  (input)         Q  u8 [M, K]  (output, e4m3 bytes)
- *   sX  f32 [M, K/128] (output)     K % 128 == 0; all pointers 16-B aligned.
+ *   sX  f32 [M, K/128] (output)     K % 16 == 0; all pointers 16-B aligned.
  */
 int fp8_quant_1x128(const float* X, uint8_t* Q, float* sX, int M, int K,
                     fp8gemm_stream_t stream);
@@ -101,7 +108,7 @@ int fp8_quant_128x128(const float* W, uint8_t* Q, float* sW, int E, int N, int K
  *   A  u8 [M, K]   sA f32 [M, K/128]
  *   B  u8 [N, K]   sB f32 [ceil(N/128), K/128]
  *   D  bf16 [M, N] (output, written in full)
- *   M >= 0, N % 8 == 0, K % 128 == 0, K > 0.
+ *   M, N >= 0; K > 0, K % 16 == 0.
  */
 int fp8gemm_dense(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
                   void* D, int M, int N, int K, fp8gemm_stream_t stream);
@@ -118,7 +125,7 @@ int fp8gemm_dense(const uint8_t* A, const float* sA, const uint8_t* B, const flo
  *      given to receive the quantised activations, e.g. to reuse them)
  *   B  u8 [N, K]   sB f32 [ceil(N/128), K/128]
  *   D  bf16 [M, N] (output, written in full)
- *   M >= 0, N % 8 == 0, K % 128 == 0, K > 0; all pointers 16-B aligned.
+ *   M, N >= 0; K > 0, K % 16 == 0; all pointers 16-B aligned.
  *
  * Two kernels on `stream`: the quantiser, then the GEMM launched as its
  * programmatic dependent, so the GEMM's launch, prologue and weight prefetch

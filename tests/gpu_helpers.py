@@ -57,8 +57,16 @@ def quantised_dense(M, N, K, kind, seed):
     from fp8_fine_grained_e4m3_gb300 import synthetic
     X, W = synthetic.dense_operands(M, N, K, kind=kind, seed=seed)
     A, sA = oquant.quant_1x128_fast(X)
-    B, sB = oquant.quant_128x128_fast(W) if N >= 1 else (np.zeros((0, K), np.uint8), None)
+    B, sB = quant_weights(W) if N >= 1 else (np.zeros((0, K), np.uint8), None)
     return A, sA, B, sB
+
+
+def quant_weights(W):
+    """The oracle's 128x128 quantiser: the vectorised form for whole K blocks,
+    the tile loop for a partial last K block."""
+    if W.shape[-1] % 128 == 0:
+        return oquant.quant_128x128_fast(W)
+    return oquant.quant_128x128(W)
 
 
 def rotated_experts(B, sB, E):

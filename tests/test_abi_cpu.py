@@ -58,7 +58,9 @@ def test_host_validation_needs_no_gpu(lib):
     good = P(1 << 20)  # never dereferenced: validation fails before any CUDA call
     s = P(0)
     assert lib.fp8gemm_dense(good, good, good, good, good, 128, 256, 200, s) == b.ERR_SHAPE
-    assert lib.fp8gemm_dense(good, good, good, good, good, 128, 250, 256, s) == b.ERR_SHAPE
+    assert lib.fp8gemm_dense(good, good, good, good, good, 128, 256, 136, s) == b.ERR_SHAPE
+    assert lib.fp8gemm_dense(good, good, good, good, good, 128, -1, 256, s) == b.ERR_SHAPE
+    assert lib.fp8gemm_dense(good, good, good, good, good, 128, 256, 0, s) == b.ERR_SHAPE
     assert lib.fp8gemm_dense(None, good, good, good, good, 128, 256, 256, s) == b.ERR_NULL
     assert lib.fp8gemm_dense(P((1 << 20) + 4), good, good, good, good, 128, 256, 256, s) == b.ERR_ALIGN
     assert lib.fp8gemm_dense(good, good, good, good, good, 0, 256, 256, s) == b.OK

@@ -41,7 +41,7 @@ def test_dense_validation_codes():
     assert L.fp8gemm_dense(_p(A), _p(sA), _p(B), _p(sB), _p(D, 8), 128, 256, 256, s) == b.ERR_ALIGN
     assert L.fp8gemm_dense(None, _p(sA), _p(B), _p(sB), _p(D), 128, 256, 256, s) == b.ERR_NULL
     assert L.fp8gemm_dense(_p(A), _p(sA), _p(B), _p(sB), _p(D), 128, 256, 200, s) == b.ERR_SHAPE
-    assert L.fp8gemm_dense(_p(A), _p(sA), _p(B), _p(sB), _p(D), 128, 252, 256, s) == b.ERR_SHAPE
+    assert L.fp8gemm_dense(_p(A), _p(sA), _p(B), _p(sB), _p(D), 128, 256, 136, s) == b.ERR_SHAPE
     assert L.fp8gemm_dense(_p(A), _p(sA), _p(B), _p(sB), _p(D), -1, 256, 256, s) == b.ERR_SHAPE
     assert b.fp8gemm_get_device_status() == b.OK
 

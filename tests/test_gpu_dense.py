@@ -39,6 +39,12 @@ def _run(A, sA, B, sB):
     (33, 2816, 768, "decode"),      # 6-CTA cluster, uneven row shares
     (20, 1536, 7168, "decode"),     # 12-CTA cluster (above the portable size)
     (2, 24576, 1536, "decode"),     # one whole tile per CTA, no split
+    (130, 256, 400, "normal"),      # partial last K block (16 of 128 columns), 256-wide tiles
+    (300, 520, 144, "prefill"),     # K = 144: two K blocks, the second 16 wide
+    (70, 1001, 208, "normal"),      # N odd: element-store epilogue; partial K block
+    (100, 2056, 1040, "prefill"),   # N >= 2048 with a partial 256-wide tile, K % 128 = 16
+    (5, 777, 400, "decode"),        # small M: partial K block, N odd
+    (48, 3000, 2064, "decode"),     # small M, clusters, partial last K block
 ])
 def test_dense_matches_oracle(M, N, K, kind):
     A, sA, B, sB = quantised_dense(M, N, K, kind, seed=M * 7 + N)

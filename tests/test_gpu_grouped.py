@@ -4,8 +4,8 @@ import numpy as np
 import pytest
 
 from fp8_fine_grained_e4m3_gb300 import synthetic
-from tests.gpu_helpers import (assert_close, dev, host, ogemm, oquant, rotated_experts,
-                               sample_rows_cols)
+from tests.gpu_helpers import (assert_close, dev, host, ogemm, oquant, quant_weights,
+                               rotated_experts, sample_rows_cols)
 
 pytestmark = pytest.mark.gpu
 
@@ -20,7 +20,7 @@ def _b():
 def _contig_case(E, T, N, K, seed, counts=None):
     X, W, lay = synthetic.contiguous_operands(E, T, N, K, seed=seed, counts=counts)
     A, sA = oquant.quant_1x128_fast(X)
-    Bq = [oquant.quant_128x128_fast(W[e]) for e in range(E)]
+    Bq = [quant_weights(W[e]) for e in range(E)]
     B = np.stack([q for q, _ in Bq])
     sB = np.stack([s for _, s in Bq])
     return A, sA, B, sB, lay
@@ -37,7 +37,8 @@ def test_contiguous_two_experts_eight_tokens():
     assert_close(got, ogemm.gemm_contiguous(A, sA, B, sB, lay.m_indices), "2x8")
 
 
-@pytest.mark.parametrize("E,T,N,K", [(5, 300, 384, 512), (8, 1000, 512, 1024), (3, 200, 2048, 256)])
+@pytest.mark.parametrize("E,T,N,K", [(5, 300, 384, 512), (8, 1000, 512, 1024), (3, 200, 2048, 256),
+                                     (4, 300, 300, 400)])  # partial last K block, N % 8 != 0
 def test_contiguous_matches_oracle(E, T, N, K):
     A, sA, B, sB, lay = _contig_case(E, T, N, K, seed=E + T)
     got = _run_contig(A, sA, B, sB, lay.m_indices)
@@ -84,8 +85,8 @@ def test_contiguous_full_size_sampled():
 def _masked_case(E, M_max, N, K, masked_m, seed):
     X, W, mm = synthetic.masked_operands(E, M_max, N, K, seed=seed, masked_m=masked_m)
     A, sA = oquant.quant_1x128_fast(X.reshape(-1, K))
-    A, sA = A.reshape(E, M_max, K), sA.reshape(E, M_max, K // 128)
-    Bq = [oquant.quant_128x128_fast(W[e]) for e in range(E)]
+    A, sA = A.reshape(E, M_max, K), sA.reshape(E, M_max, -(-K // 128))
+    Bq = [quant_weights(W[e]) for e in range(E)]
     B = np.stack([q for q, _ in Bq])
     sB = np.stack([s for _, s in Bq])
     return A, sA, B, sB, mm
@@ -107,6 +108,7 @@ def _run_masked(A, sA, B, sB, mm):
     (4, 160, 256, 256, [0, 160, 5, 129]),
     (3, 256, 512, 512, [256, 1, 128]),
     (6, 64, 2048, 384, [64, 0, 0, 63, 1, 17]),
+    (3, 200, 250, 272, [200, 7, 0]),  # partial last K block, N % 8 != 0
 ])
 def test_masked_matches_oracle_and_leaves_rows(E, M_max, N, K, mm):
     mm = np.array(mm, np.int32)
@@ -125,7 +127,7 @@ def test_masked_full_size_sampled():
     mm = synthetic.masked_counts(E, M_max, seed=0)
     X, _, _ = synthetic.masked_operands(E, M_max, 8, K, seed=0, masked_m=mm)
     A, sA = oquant.quant_1x128_fast(X.reshape(-1, K))
-    A, sA = A.reshape(E, M_max, K), sA.reshape(E, M_max, K // 128)
+    A, sA = A.reshape(E, M_max, K), sA.reshape(E, M_max, -(-K // 128))
     _, W = synthetic.dense_operands(1, N, K, kind="decode", seed=1)
     B0, sB0 = oquant.quant_128x128_fast(W)
     B, sB = rotated_experts(B0, sB0, E)

@@ -4,7 +4,7 @@ import numpy as np
 import pytest
 
 from fp8_fine_grained_e4m3_gb300 import synthetic
-from tests.gpu_helpers import dev, host, oquant
+from tests.gpu_helpers import dev, host, oquant, quant_weights
 
 pytestmark = pytest.mark.gpu
 
@@ -15,7 +15,9 @@ def _binding():
 
 
 @pytest.mark.parametrize("M,K,kind", [(128, 512, "normal"), (257, 4096, "prefill"),
-                                      (64, 7168, "decode"), (1, 128, "normal")])
+                                      (64, 7168, "decode"), (1, 128, "normal"),
+                                      (33, 144, "normal"), (5, 16, "normal"),    # partial K block
+                                      (3000, 400, "prefill")])                   # many CTAs, partial
 def test_quant_1x128_bit_exact(M, K, kind):
     X, _ = synthetic.dense_operands(M, 8, K, kind=kind, seed=M + K)
     Q, S = _binding().fp8_quant_1x128(dev(X))
@@ -67,12 +69,13 @@ def test_quant_1x128_edge_values():
     assert np.array_equal(host(S).view(np.uint32), So.view(np.uint32))
 
 
-@pytest.mark.parametrize("E,N,K", [(1, 256, 512), (1, 300, 384), (3, 520, 256), (1, 7168, 2048)])
+@pytest.mark.parametrize("E,N,K", [(1, 256, 512), (1, 300, 384), (3, 520, 256), (1, 7168, 2048),
+                                   (2, 300, 400), (1, 130, 16)])  # partial last K tile
 def test_quant_128x128_bit_exact(E, N, K):
     _, W, _ = synthetic.masked_operands(E, 1, N, K, seed=E * N + K)
     Q, S = _binding().fp8_quant_128x128(dev(W))
     for e in range(E):
-        Qo, So = oquant.quant_128x128_fast(W[e])
+        Qo, So = quant_weights(W[e])
         assert np.array_equal(host(Q)[e], Qo)
         assert np.array_equal(host(S)[e].view(np.uint32), So.view(np.uint32))
 

@@ -8,7 +8,7 @@ import numpy as np
 import pytest
 
 from fp8_fine_grained_e4m3_gb300 import synthetic
-from tests.gpu_helpers import assert_close, dev, host, ogemm, oquant
+from tests.gpu_helpers import assert_close, dev, host, ogemm, oquant, quant_weights
 
 pytestmark = pytest.mark.gpu
 
@@ -20,7 +20,7 @@ def _b():
 
 def _weights(N, K, seed):
     _, W = synthetic.dense_operands(1, N, K, kind="decode", seed=seed)
-    return oquant.quant_128x128_fast(W)
+    return quant_weights(W)
 
 
 @pytest.mark.parametrize("M,N,K", [
@@ -33,6 +33,8 @@ def _weights(N, K, seed):
     (17, 128, 16384),    # one N tile, split-K reduction
     (5, 128, 131072),    # stream-K across tile boundaries
     (200, 2304, 1024),   # large-M GEMM
+    (3, 1000, 400),      # partial last K block
+    (150, 333, 272),     # large M, N odd, partial K block
 ])
 def test_quant_a_matches_oracle_and_two_call_path(M, N, K):
     b = _b()
@@ -43,7 +45,7 @@ def test_quant_a_matches_oracle_and_two_call_path(M, N, K):
     tX, tB, tsB = dev(X), dev(Bq), dev(sB)
     import torch
     Q = torch.empty((M, K), dtype=torch.uint8, device="cuda")
-    sA = torch.empty((M, K // 128), dtype=torch.float32, device="cuda")
+    sA = torch.empty((M, -(-K // 128)), dtype=torch.float32, device="cuda")
     D = b.fp8gemm_dense_quant_a(tX, tB, tsB, Q=Q, sA=sA)
     Qo, sAo = oquant.quant_1x128_fast(X)
     assert np.array_equal(host(Q), Qo)
