@@ -18,6 +18,8 @@ Modules:
 
 * :mod:`oracle.e4m3`  -- the OCP E4M3 ("fn") code: decode table and
   round-to-nearest-even, saturating encoder.
+* :mod:`oracle.e5m2`  -- the E5M2 code (IEEE-style infinities and NaNs),
+  same two pieces.
 * :mod:`oracle.quant` -- 1x128 (activations) and 128x128 (weights)
   quantisers, FP32 semantics.
 * :mod:`oracle.gemm`  -- the block-scaled GEMM in FP64: dense, grouped
@@ -27,4 +29,4 @@ Every function is pinned by ``tests/test_oracle_*.py`` against closed forms,
 library routines or brute force; nothing here is "parity unpinned".
 """
 
-from . import e4m3, quant, gemm  # noqa: F401
+from . import e4m3, e5m2, quant, gemm  # noqa: F401

@@ -28,14 +28,24 @@ shape data lives in device memory):
 * masked: A is [E, M_max, K]; only the first masked_m[e] rows of expert e are
   computed; the other rows are not written (NaN here).
 
-Steps: decode bytes through the e4m3 table; for each K block form the block
-product with a float64 matmul (library primitive); multiply by the float64
-scale product; accumulate in float64.
+Steps: decode bytes through the format's table; for each K block form the
+block product with a float64 matmul (library primitive); multiply by the
+float64 scale product; accumulate in float64.
+
+Operand formats: A and B are e4m3 by default; either may be e5m2
+(``a_fmt`` / ``b_fmt``), e.g. an e5m2 gradient against e4m3 weights
+("news.rkmt.cn/news/5092" section 2.1; "lpnh.cn/news/2822121" section 2.1:
+mixing the two formats is allowed and costs precision).  Only the decoding of
+the bytes changes.
 """
 
 import numpy as np
 
-from .e4m3 import decode
+from . import e4m3, e5m2
+
+
+def _decoder(fmt):
+    return {"e4m3": e4m3.decode, "e5m2": e5m2.decode}[fmt]
 
 BLOCK = 128
 
@@ -55,7 +65,7 @@ def _block_scaled(Ad, sA, Bd, sB_rows) -> np.ndarray:
     return D
 
 
-def gemm_dense(A, sA, B, sB) -> np.ndarray:
+def gemm_dense(A, sA, B, sB, a_fmt="e4m3", b_fmt="e4m3") -> np.ndarray:
     """A u8 [M, K], sA f32 [M, Kb], B u8 [N, K], sB f32 [Nb, Kb] -> f64 [M, N]."""
     A = np.asarray(A, dtype=np.uint8)
     B = np.asarray(B, dtype=np.uint8)
@@ -67,18 +77,18 @@ def gemm_dense(A, sA, B, sB) -> np.ndarray:
     sB = np.asarray(sB, dtype=np.float32).astype(np.float64)
     assert sA.shape == (M, Kb) and sB.shape == (-(-N // BLOCK), Kb)
     sB_rows = sB[np.arange(N) // BLOCK]  # scale row of B row n is n // 128
-    return _block_scaled(decode(A), sA, decode(B), sB_rows)
+    return _block_scaled(_decoder(a_fmt)(A), sA, _decoder(b_fmt)(B), sB_rows)
 
 
-def gemm_dense_at(A, sA, B, sB, rows, cols) -> np.ndarray:
+def gemm_dense_at(A, sA, B, sB, rows, cols, a_fmt="e4m3", b_fmt="e4m3") -> np.ndarray:
     """D[rows][:, cols] of :func:`gemm_dense`, without forming the rest:
     D[m, n] depends only on A[m], sA[m], B[n] and sB[n // 128]."""
     rows = np.asarray(rows, dtype=np.int64)
     cols = np.asarray(cols, dtype=np.int64)
     sA = np.asarray(sA, dtype=np.float32).astype(np.float64)[rows]
     sB = np.asarray(sB, dtype=np.float32).astype(np.float64)
-    return _block_scaled(decode(np.asarray(A)[rows]), sA,
-                         decode(np.asarray(B)[cols]), sB[cols // BLOCK])
+    return _block_scaled(_decoder(a_fmt)(np.asarray(A)[rows]), sA,
+                         _decoder(b_fmt)(np.asarray(B)[cols]), sB[cols // BLOCK])
 
 
 def gemm_contiguous(A, sA, B, sB, m_indices) -> np.ndarray:

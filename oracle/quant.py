@@ -27,27 +27,36 @@ Arithmetic, in this order, all in IEEE FP32 with round-to-nearest:
 A block whose amax is 0 stores s = 0 and all-zero bytes (0x00), so that no
 0/0 is formed.  K (and N for the weight quantiser) may end in a ragged block:
 its amax runs over the elements that exist.
+
+Every function takes ``fmt`` = "e4m3" (the default, limit 448) or "e5m2"
+(limit 57344, the largest finite e5m2 value): the same rule with that
+format's limit and encoder (gradients and other wide-range tensors,
+"news.rkmt.cn/news/5092" section 2.1).
 """
 
 import numpy as np
 
-from .e4m3 import encode_rne_sat, E4M3_MAX
+from . import e4m3, e5m2
 
 BLOCK = 128
 
+_FORMATS = {"e4m3": (e4m3.E4M3_MAX, e4m3.encode_rne_sat),
+            "e5m2": (e5m2.E5M2_MAX, e5m2.encode_rne_sat)}
 
-def _quant_block(x: np.ndarray):
+
+def _quant_block(x: np.ndarray, fmt: str = "e4m3"):
     """Quantise one block (any shape) of FP32 values -> (bytes, scale)."""
+    limit, encode = _FORMATS[fmt]
     x = np.asarray(x, dtype=np.float32)
     amax = np.float32(np.max(np.abs(x))) if x.size else np.float32(0.0)
-    s = np.float32(amax / np.float32(E4M3_MAX))
+    s = np.float32(amax / np.float32(limit))
     if amax == 0:
         return np.zeros(x.shape, dtype=np.uint8), s
     y = (x / s).astype(np.float32)  # IEEE FP32 division, round to nearest
-    return encode_rne_sat(y), s
+    return encode(y), s
 
 
-def quant_1x128(X: np.ndarray):
+def quant_1x128(X: np.ndarray, fmt: str = "e4m3"):
     """Activations: X f32 [M, K] -> (Q u8 [M, K], sX f32 [M, ceil(K/128)]).
 
     One scale per row and 128-wide K block.  Loops over (row, K block) so each
@@ -62,13 +71,14 @@ def quant_1x128(X: np.ndarray):
     for m in range(M):
         for kb in range(Kb):
             sl = slice(kb * BLOCK, min(K, (kb + 1) * BLOCK))
-            Q[m, sl], S[m, kb] = _quant_block(X[m, sl])
+            Q[m, sl], S[m, kb] = _quant_block(X[m, sl], fmt)
     return Q, S
 
 
-def quant_1x128_fast(X: np.ndarray):
+def quant_1x128_fast(X: np.ndarray, fmt: str = "e4m3"):
     """Same result as :func:`quant_1x128`, one K block at a time over all rows
     (NumPy broadcasting instead of a row loop), for the large test sizes."""
+    limit, encode = _FORMATS[fmt]
     X = np.ascontiguousarray(X, dtype=np.float32)
     M, K = X.shape
     Kb = -(-K // BLOCK)
@@ -78,18 +88,18 @@ def quant_1x128_fast(X: np.ndarray):
         sl = slice(kb * BLOCK, min(K, (kb + 1) * BLOCK))
         blk = X[:, sl]
         amax = np.max(np.abs(blk), axis=1).astype(np.float32)
-        s = (amax / np.float32(E4M3_MAX)).astype(np.float32)
+        s = (amax / np.float32(limit)).astype(np.float32)
         S[:, kb] = s
         nz = amax != 0
         safe = np.where(nz, s, np.float32(1.0)).astype(np.float32)
         y = (blk / safe[:, None]).astype(np.float32)
-        q = encode_rne_sat(y)
+        q = encode(y)
         q[~nz, :] = 0
         Q[:, sl] = q
     return Q, S
 
 
-def quant_128x128(W: np.ndarray):
+def quant_128x128(W: np.ndarray, fmt: str = "e4m3"):
     """Weights: W f32 [N, K] -> (Q u8 [N, K], sW f32 [ceil(N/128), ceil(K/128)]).
 
     One scale per 128x128 tile (ragged tiles at the N and K ends allowed).
@@ -103,13 +113,14 @@ def quant_128x128(W: np.ndarray):
         rs = slice(nb * BLOCK, min(N, (nb + 1) * BLOCK))
         for kb in range(Kb):
             cs = slice(kb * BLOCK, min(K, (kb + 1) * BLOCK))
-            Q[rs, cs], S[nb, kb] = _quant_block(W[rs, cs])
+            Q[rs, cs], S[nb, kb] = _quant_block(W[rs, cs], fmt)
     return Q, S
 
 
-def quant_128x128_fast(W: np.ndarray):
+def quant_128x128_fast(W: np.ndarray, fmt: str = "e4m3"):
     """Same result as :func:`quant_128x128`, one 128-row band at a time with
     every K tile of the band handled together (for the large test sizes)."""
+    limit, encode = _FORMATS[fmt]
     W = np.ascontiguousarray(W, dtype=np.float32)
     N, K = W.shape
     assert K % BLOCK == 0, "vectorised form wants whole K blocks"
@@ -120,11 +131,11 @@ def quant_128x128_fast(W: np.ndarray):
         band = W[nb * BLOCK:min(N, (nb + 1) * BLOCK)]          # [rows, K]
         tiles = band.reshape(band.shape[0], Kb, BLOCK)          # [rows, Kb, 128]
         amax = np.abs(tiles).max(axis=(0, 2)).astype(np.float32)  # [Kb]
-        s = (amax / np.float32(E4M3_MAX)).astype(np.float32)
+        s = (amax / np.float32(limit)).astype(np.float32)
         S[nb] = s
         nz = amax != 0
         safe = np.where(nz, s, np.float32(1.0)).astype(np.float32)
-        q = encode_rne_sat((tiles / safe[None, :, None]).astype(np.float32))
+        q = encode((tiles / safe[None, :, None]).astype(np.float32))
         q[:, ~nz, :] = 0
         Q[nb * BLOCK:nb * BLOCK + band.shape[0]] = q.reshape(band.shape[0], K)
     return Q, S
@@ -137,9 +148,9 @@ def quant_128x128_grouped(W: np.ndarray):
     return np.stack(qs), np.stack(ss)
 
 
-def dequant_1x128(Q: np.ndarray, S: np.ndarray) -> np.ndarray:
+def dequant_1x128(Q: np.ndarray, S: np.ndarray, fmt: str = "e4m3") -> np.ndarray:
     """dec(q) * s per element (float64), for error-bound checks."""
-    from .e4m3 import decode
+    decode = e4m3.decode if fmt == "e4m3" else e5m2.decode
     M, K = Q.shape
     s_full = np.repeat(S.astype(np.float64), BLOCK, axis=1)[:, :K]
     return decode(Q) * s_full

@@ -58,7 +58,7 @@ def test_encoder_mutants_are_caught(monkeypatch):
 
 def test_quant_mutants_are_caught(monkeypatch):
     # reciprocal-multiply instead of division; scale = 448 / amax direction slip
-    def recip_block(x):
+    def recip_block(x, fmt="e4m3"):
         x = np.asarray(x, dtype=np.float32)
         amax = np.float32(np.max(np.abs(x)))
         s = np.float32(amax / np.float32(448))
@@ -66,7 +66,7 @@ def test_quant_mutants_are_caught(monkeypatch):
             return np.zeros(x.shape, np.uint8), s
         return e4m3.encode_rne_sat(x * np.float32(np.float32(1) / s)), s
 
-    def inverted_block(x):
+    def inverted_block(x, fmt="e4m3"):
         x = np.asarray(x, dtype=np.float32)
         amax = np.float32(np.max(np.abs(x)))
         s = np.float32(np.float32(448) / amax) if amax else np.float32(0)
