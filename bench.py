@@ -390,6 +390,26 @@ def measure_configs(peaks, dev):
             res[f"decode_quant_a_{M}x{N}x{K}"] = r
             del copies, fns, fns_q, X
 
+    # mixed formats: e5m2 A (a gradient) against e4m3 B, large and decode shapes
+    for (M, N, K) in ((4096, 7168, 16384), (16, 7168, 2048)):
+        X, W = synthetic.dense_operands_device(M, N, K, kind="prefill", seed=1, device=dev)
+        A8, sA = b.fp8_quant_1x128_fmt(X, "e5m2")
+        B8, sB = b.fp8_quant_128x128(W)
+        del X, W
+        D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        if M <= 64:
+            copies = [(B8.clone(), sB.clone()) for _ in range(24)]
+            fns = [(lambda Bc=Bc, sBc=sBc: b.fp8gemm_dense_fmt(A8, sA, "e5m2", Bc, sBc, "e4m3",
+                                                                 D=D))
+                   for Bc, sBc in copies]
+            ms = time_graph(fns, reps=4)
+            del copies, fns
+        else:
+            ms = time_launch(lambda: b.fp8gemm_dense_fmt(A8, sA, "e5m2", B8, sB, "e4m3", D=D),
+                             flush)
+        res[f"dense_e5m2xe4m3_{M}x{N}x{K}"] = _roof(2 * M * N * K, gemm_bytes(M, N, K), ms, peaks)
+        del A8, sA, B8, sB, D
+
     # quantiser on the large prefill activations
     X, _ = synthetic.dense_operands_device(4096, 8, 16384, kind="prefill", seed=0, device=dev)
     Q = torch.empty(X.shape, dtype=torch.uint8, device=dev)

@@ -26,6 +26,8 @@ ERR_LAUNCH = -5
 ERR_DEVICE_STATUS = -6
 ERR_TIMEOUT = -7
 ERR_SCRATCH_LIMIT = -8
+ERR_FORMAT = -9
+FMT = {"e4m3": 0, "e5m2": 1}  # FP8GEMM_FMT_*
 
 _lib = None
 _lock = threading.Lock()
@@ -37,6 +39,9 @@ SIGNATURES = [
     ("fp8_quant_1x128", _I, [_P, _P, _P, _I, _I, _P]),
     ("fp8_quant_128x128", _I, [_P, _P, _P, _I, _I, _I, _P]),
     ("fp8gemm_dense", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _P]),
+    ("fp8_quant_1x128_fmt", _I, [_P, _P, _P, _I, _I, _I, _P]),
+    ("fp8_quant_128x128_fmt", _I, [_P, _P, _P, _I, _I, _I, _I, _P]),
+    ("fp8gemm_dense_fmt", _I, [_P, _P, _I, _P, _P, _I, _P, _I, _I, _I, _P]),
     ("fp8gemm_dense_quant_a", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
     ("fp8gemm_grouped_contiguous", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     ("fp8gemm_grouped_masked", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
@@ -180,6 +185,63 @@ def fp8gemm_dense(A, sA, B, sB, D=None, stream=None):
         D = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
     _check(lib().fp8gemm_dense(_ptr(A), _ptr(_f32(sA, "sA")), _ptr(B), _ptr(_f32(sB, "sB")),
                                _ptr(_dev(D, "D")), M, N, K, _stream(stream)), "fp8gemm_dense")
+    return D
+
+
+def _fmt(name):
+    if name not in FMT:
+        raise ValueError(f"format must be one of {sorted(FMT)}, got {name!r}")
+    return FMT[name]
+
+
+def fp8_quant_1x128_fmt(X, fmt, Q=None, sX=None, stream=None):
+    """fp8_quant_1x128 with the output format ("e4m3" or "e5m2")."""
+    torch = _torch()
+    X = _f32(X, "X")
+    K = X.shape[-1]
+    M = X.numel() // K if K else 0
+    if Q is None:
+        Q = torch.empty(X.shape, dtype=torch.uint8, device=X.device)
+    if sX is None:
+        sX = torch.empty((*X.shape[:-1], -(-K // 128)), dtype=torch.float32, device=X.device)
+    _check(lib().fp8_quant_1x128_fmt(_ptr(X), _ptr(_u8(Q, "Q")), _ptr(_f32(sX, "sX")), M, K,
+                                     _fmt(fmt), _stream(stream)), "fp8_quant_1x128_fmt")
+    return Q, sX
+
+
+def fp8_quant_128x128_fmt(W, fmt, Q=None, sW=None, stream=None):
+    """fp8_quant_128x128 with the output format ("e4m3" or "e5m2")."""
+    torch = _torch()
+    W = _f32(W, "W")
+    squeeze = W.dim() == 2
+    W3 = W.unsqueeze(0) if squeeze else W
+    E, N, K = W3.shape
+    if Q is None:
+        Q = torch.empty(W.shape, dtype=torch.uint8, device=W.device)
+    if sW is None:
+        shp = ((N + 127) // 128, -(-K // 128))
+        sW = torch.empty(shp if squeeze else (E, *shp), dtype=torch.float32, device=W.device)
+    _check(lib().fp8_quant_128x128_fmt(_ptr(W3), _ptr(_u8(Q, "Q")), _ptr(_f32(sW, "sW")), E, N,
+                                       K, _fmt(fmt), _stream(stream)), "fp8_quant_128x128_fmt")
+    return Q, sW
+
+
+def fp8gemm_dense_fmt(A, sA, a_fmt, B, sB, b_fmt, D=None, stream=None):
+    """fp8gemm_dense with operand formats ("e4m3" / "e5m2") for A and B."""
+    torch = _torch()
+    A, B = _dev(A, "A"), _dev(B, "B")
+    if A.dtype in (torch.float8_e4m3fn, torch.float8_e5m2):
+        A = A.view(torch.uint8)
+    if B.dtype in (torch.float8_e4m3fn, torch.float8_e5m2):
+        B = B.view(torch.uint8)
+    A, B = _u8(A, "A"), _u8(B, "B")
+    M, K = A.shape
+    N = B.shape[0]
+    if D is None:
+        D = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    _check(lib().fp8gemm_dense_fmt(_ptr(A), _ptr(_f32(sA, "sA")), _fmt(a_fmt), _ptr(B),
+                                   _ptr(_f32(sB, "sB")), _fmt(b_fmt), _ptr(_dev(D, "D")), M, N,
+                                   K, _stream(stream)), "fp8gemm_dense_fmt")
     return D
 
 

@@ -174,32 +174,48 @@ void count_kernel_launches(int n) { g_launches += n; }
 
 extern "C" {
 
-int fp8_quant_1x128(const float* X, uint8_t* Q, float* sX, int M, int K,
-                    fp8gemm_stream_t stream) {
+int fp8_quant_1x128_fmt(const float* X, uint8_t* Q, float* sX, int M, int K, int fmt,
+                        fp8gemm_stream_t stream) {
   if (M < 0 || K < 0 || K % kKAlign != 0) return FP8GEMM_ERR_SHAPE;
+  if (fmt != FP8GEMM_FMT_E4M3 && fmt != FP8GEMM_FMT_E5M2) return FP8GEMM_ERR_FORMAT;
   if (M == 0 || K == 0) return FP8GEMM_OK;
   if (!X || !Q || !sX) return FP8GEMM_ERR_NULL;
   if (!aligned16(X) || !aligned16(Q) || !aligned16(sX)) return FP8GEMM_ERR_ALIGN;
   LaunchCtx c;
   if (int r = ctx_for(stream, &c)) return r;
-  return finish(launch_quant_1x128(c, X, Q, sX, M, K), 1);
+  return finish(launch_quant_1x128(c, X, Q, sX, M, K, fmt), 1);
 }
 
-int fp8_quant_128x128(const float* W, uint8_t* Q, float* sW, int E, int N, int K,
-                      fp8gemm_stream_t stream) {
+int fp8_quant_1x128(const float* X, uint8_t* Q, float* sX, int M, int K,
+                    fp8gemm_stream_t stream) {
+  return fp8_quant_1x128_fmt(X, Q, sX, M, K, FP8GEMM_FMT_E4M3, stream);
+}
+
+int fp8_quant_128x128_fmt(const float* W, uint8_t* Q, float* sW, int E, int N, int K, int fmt,
+                          fp8gemm_stream_t stream) {
   if (E < 0 || N < 0 || K < 0 || K % kKAlign != 0) return FP8GEMM_ERR_SHAPE;
+  if (fmt != FP8GEMM_FMT_E4M3 && fmt != FP8GEMM_FMT_E5M2) return FP8GEMM_ERR_FORMAT;
   if (E == 0 || N == 0 || K == 0) return FP8GEMM_OK;
   if ((long long)E * N * (long long)K > (1LL << 46)) return FP8GEMM_ERR_SHAPE;
   if (!W || !Q || !sW) return FP8GEMM_ERR_NULL;
   if (!aligned16(W) || !aligned16(Q) || !aligned16(sW)) return FP8GEMM_ERR_ALIGN;
   LaunchCtx c;
   if (int r = ctx_for(stream, &c)) return r;
-  return finish(launch_quant_128x128(c, W, Q, sW, E, N, K), 1);
+  return finish(launch_quant_128x128(c, W, Q, sW, E, N, K, fmt), 1);
 }
 
-int fp8gemm_dense(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB, void* D,
-                  int M, int N, int K, fp8gemm_stream_t stream) {
+int fp8_quant_128x128(const float* W, uint8_t* Q, float* sW, int E, int N, int K,
+                      fp8gemm_stream_t stream) {
+  return fp8_quant_128x128_fmt(W, Q, sW, E, N, K, FP8GEMM_FMT_E4M3, stream);
+}
+
+int fp8gemm_dense_fmt(const uint8_t* A, const float* sA, int a_fmt, const uint8_t* B,
+                      const float* sB, int b_fmt, void* D, int M, int N, int K,
+                      fp8gemm_stream_t stream) {
   if (int r = check_common(M, N, K)) return r;
+  if ((a_fmt != FP8GEMM_FMT_E4M3 && a_fmt != FP8GEMM_FMT_E5M2) ||
+      (b_fmt != FP8GEMM_FMT_E4M3 && b_fmt != FP8GEMM_FMT_E5M2))
+    return FP8GEMM_ERR_FORMAT;
   if (M == 0 || N == 0) return FP8GEMM_OK;
   if (!A || !sA || !B || !sB || !D) return FP8GEMM_ERR_NULL;
   if (!aligned16(A) || !aligned16(sA) || !aligned16(B) || !aligned16(sB) || !aligned16(D))
@@ -208,6 +224,8 @@ int fp8gemm_dense(const uint8_t* A, const float* sA, const uint8_t* B, const flo
   if (int r = ctx_for(stream, &c)) return r;
   GemmArgs a{GemmMode::kDense, A, sA, B, sB, nullptr, static_cast<__nv_bfloat16*>(D),
              M, N, K, 1};
+  a.a_fmt = a_fmt;
+  a.b_fmt = b_fmt;
   if (M <= kSmallM) {
     if (!small_m_uses_workspace(c, a)) return finish(launch_gemm_small_m_any(c, a, nullptr, 0), 1);
     const size_t bytes = small_m_workspace_bytes(c.num_sms, N);
@@ -216,6 +234,12 @@ int fp8gemm_dense(const uint8_t* A, const float* sA, const uint8_t* B, const flo
     return finish(launch_gemm_small_m_any(c, a, ws, bytes), 1);
   }
   return finish(launch_gemm_tc(c, a), 1);
+}
+
+int fp8gemm_dense(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB, void* D,
+                  int M, int N, int K, fp8gemm_stream_t stream) {
+  return fp8gemm_dense_fmt(A, sA, FP8GEMM_FMT_E4M3, B, sB, FP8GEMM_FMT_E4M3, D, M, N, K,
+                           stream);
 }
 
 int fp8gemm_dense_quant_a(const float* X, uint8_t* Q, float* sA, const uint8_t* B,
@@ -307,6 +331,7 @@ const char* fp8gemm_strerror(int code) {
     case FP8GEMM_ERR_TIMEOUT: return "a pipeline wait exceeded its time limit";
     case FP8GEMM_ERR_SCRATCH_LIMIT:
       return "problem exceeds the fixed scratch of fp8gemm_dense_small_m_noalloc (M <= 64)";
+    case FP8GEMM_ERR_FORMAT: return "unknown FP8 format (FP8GEMM_FMT_E4M3 or FP8GEMM_FMT_E5M2)";
     default: return "unknown status";
   }
 }

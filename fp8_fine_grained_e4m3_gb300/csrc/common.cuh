@@ -33,9 +33,9 @@ struct LaunchCtx {
 };
 
 cudaError_t launch_quant_1x128(const LaunchCtx& c, const float* X, uint8_t* Q, float* sX,
-                               int M, int K);
+                               int M, int K, int fmt = FP8GEMM_FMT_E4M3);
 cudaError_t launch_quant_128x128(const LaunchCtx& c, const float* W, uint8_t* Q, float* sW,
-                                 int E, int N, int K);
+                                 int E, int N, int K, int fmt = FP8GEMM_FMT_E4M3);
 
 // Problem description for the persistent tensor-core GEMM.
 enum class GemmMode : int { kDense = 0, kContiguous = 1, kMasked = 2 };
@@ -51,6 +51,8 @@ struct GemmArgs {
   int M;      // dense: M; contiguous: M_pad; masked: M_max (rows per expert)
   int N, K;
   int E;      // experts (1 for dense)
+  int a_fmt = FP8GEMM_FMT_E4M3;  // operand formats (tensor-core type codes: e4m3 0, e5m2 1)
+  int b_fmt = FP8GEMM_FMT_E4M3;
 };
 
 cudaError_t launch_gemm_tc(const LaunchCtx& c, const GemmArgs& a);

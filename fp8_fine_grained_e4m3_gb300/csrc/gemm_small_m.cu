@@ -191,7 +191,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 2)
   } else if (warp == Cfg::kMmaWarp) {
     // ------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_e4m3_f32(128, MP);
+      // swap-AB: the MMA's A operand is the weights (the GEMM's B), its B
+      // operand the activations
+      const uint32_t idesc = idesc_f8_f32(128, MP, uint32_t(args.b_fmt), uint32_t(args.a_fmt));
       const uint32_t w_base = smem_addr(smW);
       const uint32_t x_base = smem_addr(smX);
       int i = 0;

@@ -262,7 +262,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     // ------------------------------------------------------ MMA issuer
     regs_decrease<Cfg::kLowRegs>();
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_e4m3_f32(kBlockM, BN);
+      const uint32_t idesc =
+          idesc_f8_f32(kBlockM, BN, uint32_t(args.a_fmt), uint32_t(args.b_fmt));
       const uint32_t a_base = smem_addr(smA);
       const uint32_t b_base = smem_addr(smB);
       uint32_t it = 0;

@@ -193,6 +193,13 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t M, uint32_t N) {
   return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
+// The same with the MMA's A and B operand formats set (kind::f8f6f4 type
+// codes: E4M3 = 0, E5M2 = 1; A at bits 7-9, B at bits 10-12).
+__host__ __device__ constexpr uint32_t idesc_f8_f32(uint32_t M, uint32_t N, uint32_t a_type,
+                                                    uint32_t b_type) {
+  return idesc_e4m3_f32(M, N) | (a_type << 7) | (b_type << 10);
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T, one instruction of K = 32 (8-bit types).
 __device__ __forceinline__ void umma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                           uint32_t idesc, uint32_t accumulate) {

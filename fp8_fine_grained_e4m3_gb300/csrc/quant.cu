@@ -17,18 +17,30 @@
 namespace fp8gemm {
 namespace {
 
-// Two FP32 values -> two e4m3 bytes (lo in the low byte), round to nearest
-// even, saturate to +-448.
-__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+// Two FP32 values -> two FP8 bytes (lo in the low byte), round to nearest
+// even, saturate to the format's largest finite value (+-448 e4m3, +-57344
+// e5m2).
+template <bool kE5M2>
+__device__ __forceinline__ uint32_t cvt_f8x2(float lo, float hi) {
   uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  if constexpr (kE5M2)
+    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  else
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
 }
 
+template <bool kE5M2>
 __device__ __forceinline__ uint32_t quant4(float4 v, float s) {
   const float q0 = __fdiv_rn(v.x, s), q1 = __fdiv_rn(v.y, s);
   const float q2 = __fdiv_rn(v.z, s), q3 = __fdiv_rn(v.w, s);
-  return cvt_e4m3x2(q0, q1) | (cvt_e4m3x2(q2, q3) << 16);
+  return cvt_f8x2<kE5M2>(q0, q1) | (cvt_f8x2<kE5M2>(q2, q3) << 16);
+}
+
+// The format's largest finite value: the divisor of the scale rule.
+template <bool kE5M2>
+__device__ __forceinline__ float f8_limit() {
+  return kE5M2 ? 57344.0f : kE4M3Max;
 }
 
 __device__ __forceinline__ float absmax4(float4 v) {
@@ -44,7 +56,7 @@ constexpr int kQuantUnroll = 4;  // 1x128 blocks per warp (loads kept in flight)
 // K % 128 remaining elements (a multiple of 16) and its amax runs over those.
 // kPdl: launched as a programmatic dependent of the previous kernel (wait for
 // it before the first load; let the next kernel launch right away).
-template <bool kPdl, bool kRagged>
+template <bool kPdl, bool kRagged, bool kE5M2>
 __global__ void __launch_bounds__(256) quant_1x128_kernel(const float* __restrict__ X,
                                                           uint32_t* __restrict__ Q,
                                                           float* __restrict__ sX,
@@ -81,8 +93,8 @@ __global__ void __launch_bounds__(256) quant_1x128_kernel(const float* __restric
     float amax = absmax4(v[u]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float s = __fdiv_rn(amax, kE4M3Max);
-    if (in[u]) Q[e0[u] / 4 + lane] = amax != 0.f ? quant4(v[u], s) : 0u;
+    const float s = __fdiv_rn(amax, f8_limit<kE5M2>());
+    if (in[u]) Q[e0[u] / 4 + lane] = amax != 0.f ? quant4<kE5M2>(v[u], s) : 0u;
     if (lane == 0) sX[b] = s;
   }
 }
@@ -90,6 +102,7 @@ __global__ void __launch_bounds__(256) quant_1x128_kernel(const float* __restric
 // One CTA (256 threads) per 128x128 tile of one [N, K] matrix of the batch.
 // Thread t covers column group t % 32 (4 columns) of rows t / 32 + 8 i.
 // The last K tile may be partial (K % 128 columns, a multiple of 16).
+template <bool kE5M2>
 __global__ void __launch_bounds__(256) quant_128x128_kernel(const float* __restrict__ W,
                                                             uint8_t* __restrict__ Q,
                                                             float* __restrict__ sW, int N,
@@ -124,13 +137,13 @@ __global__ void __launch_bounds__(256) quant_128x128_kernel(const float* __restr
   amax = red[0];
 #pragma unroll
   for (int w = 1; w < 8; ++w) amax = fmaxf(amax, red[w]);
-  const float s = __fdiv_rn(amax, kE4M3Max);
+  const float s = __fdiv_rn(amax, f8_limit<kE5M2>());
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const int n = nb * 128 + r0 + 8 * i;
     if (n < N && col_in) {
       uint32_t* dst = reinterpret_cast<uint32_t*>(Q + mat + size_t(n) * K + kb * kBlockK) + cg;
-      *dst = amax != 0.f ? quant4(v[i], s) : 0u;
+      *dst = amax != 0.f ? quant4<kE5M2>(v[i], s) : 0u;
     }
   }
   if (threadIdx.x == 0) sW[(size_t(e) * Nb + nb) * Kb + kb] = s;
@@ -138,8 +151,11 @@ __global__ void __launch_bounds__(256) quant_128x128_kernel(const float* __restr
 
 }  // namespace
 
-cudaError_t launch_quant_1x128(const LaunchCtx& c, const float* X, uint8_t* Q, float* sX,
-                               int M, int K) {
+namespace {
+
+template <bool kE5M2>
+cudaError_t launch_1x128(const LaunchCtx& c, const float* X, uint8_t* Q, float* sX, int M,
+                         int K) {
   const int Kb = ceil_div(K, kBlockK);
   const long long nblocks = (long long)M * Kb;
   if (nblocks == 0) return cudaSuccess;
@@ -150,11 +166,11 @@ cudaError_t launch_quant_1x128(const LaunchCtx& c, const float* X, uint8_t* Q, f
   uint32_t* Q4 = reinterpret_cast<uint32_t*>(Q);
   if (grid > 8LL * c.num_sms) {  // more than one wave: plain launch
     if (ragged)
-      quant_1x128_kernel<false, true><<<unsigned(grid), 256, 0, c.stream>>>(X, Q4, sX, nblocks,
-                                                                             K, Kb);
+      quant_1x128_kernel<false, true, kE5M2>
+          <<<unsigned(grid), 256, 0, c.stream>>>(X, Q4, sX, nblocks, K, Kb);
     else
-      quant_1x128_kernel<false, false><<<unsigned(grid), 256, 0, c.stream>>>(X, Q4, sX, nblocks,
-                                                                              K, Kb);
+      quant_1x128_kernel<false, false, kE5M2>
+          <<<unsigned(grid), 256, 0, c.stream>>>(X, Q4, sX, nblocks, K, Kb);
     return cudaGetLastError();
   }
   // A decode-sized quantisation (one wave) is launched as a programmatic
@@ -171,17 +187,30 @@ cudaError_t launch_quant_1x128(const LaunchCtx& c, const float* X, uint8_t* Q, f
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   if (ragged)
-    return cudaLaunchKernelEx(&cfg, quant_1x128_kernel<true, true>, X, Q4, sX, nblocks, K, Kb);
-  return cudaLaunchKernelEx(&cfg, quant_1x128_kernel<true, false>, X, Q4, sX, nblocks, K, Kb);
+    return cudaLaunchKernelEx(&cfg, quant_1x128_kernel<true, true, kE5M2>, X, Q4, sX, nblocks,
+                              K, Kb);
+  return cudaLaunchKernelEx(&cfg, quant_1x128_kernel<true, false, kE5M2>, X, Q4, sX, nblocks,
+                            K, Kb);
+}
+
+}  // namespace
+
+cudaError_t launch_quant_1x128(const LaunchCtx& c, const float* X, uint8_t* Q, float* sX,
+                               int M, int K, int fmt) {
+  return fmt == FP8GEMM_FMT_E5M2 ? launch_1x128<true>(c, X, Q, sX, M, K)
+                                 : launch_1x128<false>(c, X, Q, sX, M, K);
 }
 
 cudaError_t launch_quant_128x128(const LaunchCtx& c, const float* W, uint8_t* Q, float* sW,
-                                 int E, int N, int K) {
+                                 int E, int N, int K, int fmt) {
   if (E == 0 || N == 0 || K == 0) return cudaSuccess;
   const int Nb = ceil_div(N, 128);
   if (Nb > 65535 || E > 65535) return cudaErrorInvalidValue;
   dim3 grid(ceil_div(K, kBlockK), Nb, E);
-  quant_128x128_kernel<<<grid, 256, 0, c.stream>>>(W, Q, sW, N, K);
+  if (fmt == FP8GEMM_FMT_E5M2)
+    quant_128x128_kernel<true><<<grid, 256, 0, c.stream>>>(W, Q, sW, N, K);
+  else
+    quant_128x128_kernel<false><<<grid, 256, 0, c.stream>>>(W, Q, sW, N, K);
   return cudaGetLastError();
 }
 

@@ -70,7 +70,18 @@ enum fp8gemm_status {
   FP8GEMM_ERR_LAUNCH = -5,
   FP8GEMM_ERR_DEVICE_STATUS = -6,
   FP8GEMM_ERR_TIMEOUT = -7,
-  FP8GEMM_ERR_SCRATCH_LIMIT = -8
+  FP8GEMM_ERR_SCRATCH_LIMIT = -8,
+  FP8GEMM_ERR_FORMAT = -9
+};
+
+/* FP8 operand formats of the *_fmt calls ("news.rkmt.cn/news/5092" section
+ * 2.1: e4m3 -- 4 exponent, 3 mantissa bits, largest finite 448 -- for
+ * activations and weights; e5m2 -- 5 exponent, 2 mantissa bits, IEEE-style
+ * infinities and NaNs, largest finite 57344 -- for gradients and other
+ * wide-range tensors).  Any other value returns FP8GEMM_ERR_FORMAT. */
+enum fp8gemm_format {
+  FP8GEMM_FMT_E4M3 = 0,
+  FP8GEMM_FMT_E5M2 = 1
 };
 
 /*
@@ -102,6 +113,18 @@ int fp8_quant_128x128(const float* W, uint8_t* Q, float* sW, int E, int N, int K
                       fp8gemm_stream_t stream);
 
 /*
+ * fp8_quant_1x128_fmt / fp8_quant_128x128_fmt -- fp8_quant_1x128 and
+ * fp8_quant_128x128 with the output format chosen: the same rule with the
+ * format's largest finite value as the limit (s = amax / 448 for e4m3,
+ * amax / 57344 for e5m2) and its round-to-nearest-even, saturating encoding.
+ * FP8GEMM_FMT_E4M3 gives exactly the bytes and scales of the plain calls.
+ */
+int fp8_quant_1x128_fmt(const float* X, uint8_t* Q, float* sX, int M, int K, int fmt,
+                        fp8gemm_stream_t stream);
+int fp8_quant_128x128_fmt(const float* W, uint8_t* Q, float* sW, int E, int N, int K, int fmt,
+                          fp8gemm_stream_t stream);
+
+/*
  * fp8gemm_dense -- D = A * B^T with block scales ("lpnh.cn/news/2822121"
  * section 4.1 dense main loop; scaling as above).
  *
@@ -112,6 +135,18 @@ int fp8_quant_128x128(const float* W, uint8_t* Q, float* sW, int E, int N, int K
  */
 int fp8gemm_dense(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
                   void* D, int M, int N, int K, fp8gemm_stream_t stream);
+
+/*
+ * fp8gemm_dense_fmt -- fp8gemm_dense with each operand's format given
+ * (a_fmt, b_fmt: FP8GEMM_FMT_*), e.g. an e5m2 gradient against e4m3
+ * weights; mixing the formats is allowed ("lpnh.cn/news/2822121" section
+ * 2.1).  The tensor cores decode each operand in its own format; scaling,
+ * promotion, layouts and limits are those of fp8gemm_dense.  Operand bytes
+ * that encode infinity or NaN (e5m2) propagate as in IEEE arithmetic.
+ */
+int fp8gemm_dense_fmt(const uint8_t* A, const float* sA, int a_fmt, const uint8_t* B,
+                      const float* sB, int b_fmt, void* D, int M, int N, int K,
+                      fp8gemm_stream_t stream);
 
 /*
  * fp8gemm_dense_quant_a -- fp8gemm_dense on FP32 activations: A and sA are

@@ -75,6 +75,12 @@ def test_host_validation_needs_no_gpu(lib):
                                      4, 256, 256, s) == b.ERR_ALIGN
     assert lib.fp8gemm_dense_quant_a(good, None, None, good, good, good, 0, 256, 256, s) == b.OK
     assert lib.fp8_quant_1x128(good, good, good, 4, 130, s) == b.ERR_SHAPE
+    assert lib.fp8_quant_1x128_fmt(good, good, good, 4, 256, 2, s) == b.ERR_FORMAT
+    assert lib.fp8_quant_128x128_fmt(good, good, good, 1, 256, 256, -1, s) == b.ERR_FORMAT
+    assert lib.fp8gemm_dense_fmt(good, good, 0, good, good, 5, good, 4, 256, 256, s) == b.ERR_FORMAT
+    assert lib.fp8gemm_dense_fmt(good, good, 1, good, good, 1, good, 4, 256, 136, s) == b.ERR_SHAPE
+    assert lib.fp8gemm_dense_fmt(None, good, 1, good, good, 0, good, 4, 256, 256, s) == b.ERR_NULL
+    assert b.strerror(b.ERR_FORMAT).startswith("unknown FP8 format")
     assert lib.fp8_quant_128x128(good, None, good, 1, 8, 128, s) == b.ERR_NULL
     assert lib.fp8gemm_get_device_status(s, None) == b.ERR_NULL
     assert isinstance(lib.fp8gemm_num_kernel_launches(), int)
