@@ -464,6 +464,31 @@ def measure_configs(peaks, dev):
     res["moe_masked_E16_M256_N4096_K7168"] = r
     del A8, sA, B8, sB, D
     torch.cuda.empty_cache()
+
+    # Batched decode from a device problem table: 16 problems (one per
+    # expert), M_e ~ U{1..16} tokens, N=4096, K=7168; the masked grouped
+    # kernel on the same operands beside it
+    E, M_max, N, K = 16, 16, 4096, 7168
+    mm = (synthetic.masked_counts(E, M_max - 1, seed=3) + 1).astype(np.int32)
+    X = synthetic.masked_activations_device(E, M_max, K, seed=3, device=dev)
+    A8, sA = b.fp8_quant_1x128(X)
+    del X
+    W = synthetic.expert_weights_device(E, N, K, seed=4, device=dev)
+    B8, sB = b.fp8_quant_128x128(W)
+    del W
+    D = torch.empty((E, M_max, N), dtype=torch.bfloat16, device=dev)
+    probs = [(A8[e, :mm[e]], sA[e, :mm[e]], B8[e], sB[e], D[e, :mm[e]]) for e in range(E)]
+    table = b.problem_table(probs)
+    ms_t = time_launch(lambda: b.fp8gemm_grouped_table(table, E, M_max), flush)
+    mmd = torch.from_numpy(mm).to(dev)
+    ms_m = time_launch(lambda: b.fp8gemm_grouped_masked(A8, sA, B8, sB, mmd, D=D), flush)
+    rows = int(mm.sum())
+    nbytes = gemm_bytes(rows, N, K, e_active=E, rows=rows) + 56 * E
+    r = _roof(2.0 * rows * N * K, nbytes, ms_t, peaks)
+    r["note"] = f"sum(M_e) = {rows}; fp8gemm_grouped_masked on the same operands: {ms_m * 1e3:.2f} us"
+    res["table_E16_M1-16_N4096_K7168"] = r
+    del A8, sA, B8, sB, D, table, probs
+    torch.cuda.empty_cache()
     if b.fp8gemm_get_device_status() != b.OK:
         raise RuntimeError("device status set while measuring the other workloads")
     return res

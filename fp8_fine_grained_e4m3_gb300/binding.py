@@ -42,6 +42,7 @@ SIGNATURES = [
     ("fp8_quant_1x128_fmt", _I, [_P, _P, _P, _I, _I, _I, _P]),
     ("fp8_quant_128x128_fmt", _I, [_P, _P, _P, _I, _I, _I, _I, _P]),
     ("fp8gemm_dense_fmt", _I, [_P, _P, _I, _P, _P, _I, _P, _I, _I, _I, _P]),
+    ("fp8gemm_grouped_table", _I, [_P, _I, _I, _P]),
     ("fp8gemm_dense_quant_a", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
     ("fp8gemm_grouped_contiguous", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     ("fp8gemm_grouped_masked", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
@@ -263,6 +264,40 @@ def fp8gemm_dense_quant_a(X, B, sB, D=None, Q=None, sA=None, stream=None):
                                        _ptr(_dev(D, "D")), M, N, K, _stream(stream)),
            "fp8gemm_dense_quant_a")
     return D
+
+
+class Problem(ctypes.Structure):
+    """One entry of the fp8gemm_grouped_table problem table (C layout)."""
+    _fields_ = [("A", _P), ("sA", _P), ("B", _P), ("sB", _P), ("D", _P),
+                ("M", ctypes.c_int), ("N", ctypes.c_int), ("K", ctypes.c_int),
+                ("reserved", ctypes.c_int)]
+
+
+def problem_table(problems, out=None):
+    """Device table for fp8gemm_grouped_table from (A, sA, B, sB, D) tensor
+    tuples: a uint8 CUDA tensor of len(problems) * sizeof(Problem) bytes
+    (written into `out` when given, e.g. to update a table a graph captured)."""
+    torch = _torch()
+    arr = (Problem * len(problems))()
+    for e, (A, sA, B, sB, D) in zip(arr, problems):
+        A, B = _u8(A, "A"), _u8(B, "B")
+        e.A, e.sA, e.B = A.data_ptr(), _f32(sA, "sA").data_ptr(), B.data_ptr()
+        e.sB, e.D = _f32(sB, "sB").data_ptr(), _dev(D, "D").data_ptr()
+        e.M, e.K = A.shape
+        e.N = B.shape[0]
+        e.reserved = 0
+    host = torch.frombuffer(bytearray(bytes(arr)), dtype=torch.uint8)
+    if out is None:
+        return host.to("cuda")
+    out.copy_(host)
+    return out
+
+
+def fp8gemm_grouped_table(table, num_problems, max_M, stream=None):
+    """Run every problem of a device table (see problem_table); max_M bounds
+    every entry's M (<= 64) and picks the kernel's padded width."""
+    _check(lib().fp8gemm_grouped_table(_ptr(_dev(table, "table")), int(num_problems),
+                                       int(max_M), _stream(stream)), "fp8gemm_grouped_table")
 
 
 def fp8gemm_grouped_contiguous(A, sA, B, sB, m_indices, D=None, stream=None):

@@ -15,7 +15,7 @@ ROOT = os.path.dirname(PKG_DIR)
 CSRC = os.path.join(PKG_DIR, "csrc")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libfp8gemm.so")
-SOURCES = ["quant.cu", "gemm_tc.cu", "gemm_small_m.cu", "noalloc.cu", "api.cu"]
+SOURCES = ["quant.cu", "gemm_tc.cu", "gemm_small_m.cu", "gemm_table.cu", "noalloc.cu", "api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]

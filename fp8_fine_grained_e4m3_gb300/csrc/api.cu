@@ -267,6 +267,17 @@ int fp8gemm_dense_quant_a(const float* X, uint8_t* Q, float* sA, const uint8_t* 
   return fp8gemm_dense(Q, sA, B, sB, D, M, N, K, stream);
 }
 
+int fp8gemm_grouped_table(const fp8gemm_problem* problems, int num_problems, int max_M,
+                          fp8gemm_stream_t stream) {
+  if (num_problems < 0 || max_M < 1 || max_M > kSmallM) return FP8GEMM_ERR_SHAPE;
+  if (num_problems == 0) return FP8GEMM_OK;
+  if (!problems) return FP8GEMM_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(problems) & 7u) return FP8GEMM_ERR_ALIGN;
+  LaunchCtx c;
+  if (int r = ctx_for(stream, &c)) return r;
+  return finish(launch_gemm_table(c, problems, num_problems, max_M), 1);
+}
+
 int fp8gemm_grouped_contiguous(const uint8_t* A, const float* sA, const uint8_t* B,
                                const float* sB, const int32_t* m_indices, void* D, int M_pad,
                                int N, int K, int E, fp8gemm_stream_t stream) {

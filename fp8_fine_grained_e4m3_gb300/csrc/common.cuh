@@ -65,6 +65,9 @@ bool small_m_uses_workspace(const LaunchCtx& c, const GemmArgs& a);
 cudaError_t launch_gemm_small_m_any(const LaunchCtx& c, const GemmArgs& a, void* ws,
                                     size_t ws_bytes);
 
+// Many decode-sized problems from a device-resident table (gemm_table.cu).
+cudaError_t launch_gemm_table(const LaunchCtx& c, const fp8gemm_problem* tab, int P, int max_M);
+
 // Fills `c` for the current device and `stream` (SM count, status word);
 // returns an fp8gemm_status code.  Defined in api.cu.
 int make_launch_ctx(cudaStream_t stream, LaunchCtx* c);

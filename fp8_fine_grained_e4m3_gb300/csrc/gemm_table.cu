@@ -1,0 +1,376 @@
+// gemm_table.cu -- block-scaled FP8 GEMMs of many independent decode-sized
+// problems in one launch, each problem's pointers and sizes read from a table
+// in device memory (sm_103a).
+//
+// "bhfrc.com/news/60211" sections 4.2-4.3 and 6: a grouped call takes a list
+// of problems whose shape data sit in device memory, so that one captured
+// CUDA graph can be replayed with new shapes.  Here the launch shape depends
+// only on the problem count and the largest M (the host's arguments); every
+// pointer and size comes from the table on the device, and so does every
+// check of it.
+//
+// Per problem p the arithmetic is fp8gemm_dense's (1x128 A scales, 128x128 B
+// scales, each K block contracted on the tensor cores and promoted into an
+// FP32 accumulator, BF16 out).  The decode layout of gemm_small_m.cu: swap-AB
+// (a 128-row weight tile is the MMA's M, the problem's M <= 64 rows padded to
+// MP its N), one TMEM partial per K block, promotion per output column.
+//
+// What differs: no tensor maps (they would have to be rebuilt per problem on
+// the device), so the producer warp fills the 128-byte-swizzled operand
+// stages with 16-byte cp.async copies -- zero-filled past a problem's N, M or
+// K -- and publishes each stage after its copies complete (wait_group, proxy
+// fence, mbarrier arrive, two stages behind).  Work items are (problem, N
+// tile) pairs with the whole K range, taken by persistent CTAs in a fixed
+// order that every role walks identically.
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace fp8gemm {
+namespace {
+
+template <int MP_>
+struct TabCfg {
+  static constexpr int MP = MP_;
+  static constexpr int kStages = 6;
+  static constexpr int kLag = 2;  // a stage is published kLag stages after it is issued
+  static constexpr int kThreads = 192;
+  static constexpr int kLoadWarp = 4;
+  static constexpr int kMmaWarp = 5;
+  static constexpr int kWBytes = 128 * kBlockK;
+  static constexpr int kXBytes = MP * kBlockK;
+  static constexpr int kTmemBufs = MP == 64 ? 4 : 8;
+  static constexpr int kTmemCols = kTmemBufs * MP < 128 ? 128 : kTmemBufs * MP;
+  static constexpr int kScaleKb = 16;
+  static constexpr int kBarBytes = 512;
+  static constexpr int kAuxBytes = kBarBytes + kScaleKb * (MP + 4) * 4;
+  static constexpr size_t kSmemBytes =
+      1024 + size_t(kStages) * (kWBytes + kXBytes) + kAuxBytes;
+  static_assert(kStages > kLag, "publishing lag");
+  static_assert((2 * kStages + 2 * kTmemBufs + 4) * 8 + 16 <= kBarBytes, "barrier area");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+};
+
+// A problem as the kernels use it: its table entry, or an empty problem if
+// the entry breaks the contract (then `bad` is set).
+struct Prob {
+  const uint8_t* A;
+  const float* sA;
+  const uint8_t* B;
+  const float* sB;
+  __nv_bfloat16* D;
+  int M, N, K, Kb, tiles;
+  bool bad;
+};
+
+__device__ __forceinline__ bool al16(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+__device__ Prob load_problem(const fp8gemm_problem* tab, int p, int max_M) {
+  Prob r;
+  const fp8gemm_problem* e = tab + p;
+  r.A = reinterpret_cast<const uint8_t*>(__ldg(reinterpret_cast<const unsigned long long*>(&e->A)));
+  r.sA = reinterpret_cast<const float*>(__ldg(reinterpret_cast<const unsigned long long*>(&e->sA)));
+  r.B = reinterpret_cast<const uint8_t*>(__ldg(reinterpret_cast<const unsigned long long*>(&e->B)));
+  r.sB = reinterpret_cast<const float*>(__ldg(reinterpret_cast<const unsigned long long*>(&e->sB)));
+  r.D = reinterpret_cast<__nv_bfloat16*>(__ldg(reinterpret_cast<const unsigned long long*>(&e->D)));
+  r.M = __ldg(&e->M);
+  r.N = __ldg(&e->N);
+  r.K = __ldg(&e->K);
+  const bool empty = r.M == 0 || r.N == 0;
+  r.bad = r.M < 0 || r.N < 0 || r.M > max_M || r.K <= 0 || r.K % 16 != 0 ||
+          (!empty && (!r.A || !r.sA || !r.B || !r.sB || !r.D || !al16(r.A) || !al16(r.B) ||
+                      (reinterpret_cast<uintptr_t>(r.sA) & 3u) ||
+                      (reinterpret_cast<uintptr_t>(r.sB) & 3u) ||
+                      (reinterpret_cast<uintptr_t>(r.D) & 1u)));
+  r.Kb = r.bad ? 0 : ceil_div(r.K, kBlockK);
+  r.tiles = (r.bad || empty) ? 0 : ceil_div(r.N, 128);
+  return r;
+}
+
+// The (problem, N tile) items of this CTA, in order: item = blockIdx.x +
+// j * gridDim.x over the concatenation of every problem's tiles.
+struct Walk {
+  const fp8gemm_problem* tab;
+  int P, max_M;
+  int p = -1;
+  long long first = 0;  // index of problem p's first item
+  Prob cur;
+  // Moves to the problem holding `item`; false past the last one.
+  __device__ bool seek(long long item) {
+    if (p < 0) {
+      p = 0;
+      if (P > 0) cur = load_problem(tab, 0, max_M);
+    }
+    while (p < P && item >= first + cur.tiles) {
+      first += cur.tiles;
+      if (++p < P) cur = load_problem(tab, p, max_M);
+    }
+    return p < P;
+  }
+};
+
+template <class Cfg>
+__global__ void __launch_bounds__(Cfg::kThreads, 1)
+    gemm_table_kernel(const fp8gemm_problem* __restrict__ tab, int P, int max_M, int* status) {
+  constexpr int MP = Cfg::MP;
+  constexpr int kStages = Cfg::kStages;
+  constexpr int NB = Cfg::kTmemBufs;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smW = smem;
+  uint8_t* smX = smem + kStages * Cfg::kWBytes;
+  uint8_t* aux = smX + kStages * Cfg::kXBytes;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(aux);
+  uint64_t* empty_bar = full_bar + kStages;
+  uint64_t* tfull_bar = full_bar + 2 * kStages;
+  uint64_t* tempty_bar = tfull_bar + NB;
+  uint64_t* drain_bar = tempty_bar + NB;
+  uint64_t* group_bar = drain_bar + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(group_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  float* sa_s = reinterpret_cast<float*>(aux + Cfg::kBarBytes);
+  float* sb_s = sa_s + Cfg::kScaleKb * MP;
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full_bar[s], 32);  // every lane of the producer warp
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < NB; ++b) {
+      mbar_init(&tfull_bar[b], 1);
+      mbar_init(&tempty_bar[b], 4);
+    }
+    mbar_init(drain_bar, 1);
+    mbar_init(group_bar, 128);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == Cfg::kMmaWarp) {
+    tmem_alloc(tmem_holder, Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  auto fail = [&]() {
+    *abort_flag = 1;
+    raise_status(status, FP8GEMM_ERR_TIMEOUT);
+  };
+  griddep_wait();  // the table and the operands belong to the stream's order
+
+  if (warp == Cfg::kLoadWarp) {
+    // ------------------------------------------------------ producer
+    // 8 lanes per 128-byte row (one 16-byte chunk each), 4 rows per copy
+    // instruction; chunk c of tile row r lands at r * 128 + ((c ^ (r % 8)) * 16)
+    const int c = lane % 8, r0 = lane / 8;
+    Walk w{tab, P, max_M};
+    int i = 0;  // unit (K block) counter
+    bool ok = true;
+    for (long long item = blockIdx.x; ok && w.seek(item); item += gridDim.x) {
+      const Prob& q = w.cur;
+      const int tile = int(item - w.first);
+      for (int kb = 0; kb < q.Kb; ++kb, ++i) {
+        const int s = i % kStages;
+        if (!mbar_wait(&empty_bar[s], ((i / kStages) & 1) ^ 1, abort_flag)) {
+          fail();
+          ok = false;
+          break;
+        }
+        const bool k_in = kb * kBlockK + c * 16 < q.K;
+        const uint32_t w_dst = smem_addr(smW + s * Cfg::kWBytes);
+#pragma unroll 4
+        for (int r = r0; r < 128; r += 4) {
+          const int n = tile * 128 + r;
+          const bool in = k_in && n < q.N;
+          const uint8_t* src = in ? q.B + size_t(n) * q.K + kb * kBlockK + c * 16 : q.B;
+          cp_async_16(w_dst + r * 128 + ((c ^ (r & 7)) << 4), src, in ? 16u : 0u);
+        }
+        const uint32_t x_dst = smem_addr(smX + s * Cfg::kXBytes);
+#pragma unroll
+        for (int r = r0; r < MP; r += 4) {
+          const bool in = k_in && r < q.M;
+          const uint8_t* src = in ? q.A + size_t(r) * q.K + kb * kBlockK + c * 16 : q.A;
+          cp_async_16(x_dst + r * 128 + ((c ^ (r & 7)) << 4), src, in ? 16u : 0u);
+        }
+        cp_async_commit();
+        if (i >= Cfg::kLag) {  // unit i - kLag has landed: publish it
+          cp_async_wait_group<Cfg::kLag>();
+          fence_proxy_async_smem();
+          mbar_arrive(&full_bar[(i - Cfg::kLag) % kStages]);
+        }
+      }
+    }
+    cp_async_wait_group<0>();  // publish the last units (all copies land)
+    fence_proxy_async_smem();
+    for (int j = i - Cfg::kLag < 0 ? 0 : i - Cfg::kLag; j < i; ++j)
+      mbar_arrive(&full_bar[j % kStages]);
+  } else if (warp == Cfg::kMmaWarp) {
+    // ------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_e4m3_f32(128, MP);
+      const uint32_t w_base = smem_addr(smW);
+      const uint32_t x_base = smem_addr(smX);
+      Walk w{tab, P, max_M};
+      int i = 0;
+      bool ok = true;
+      for (long long item = blockIdx.x; ok && w.seek(item); item += gridDim.x) {
+        for (int kb = 0; kb < w.cur.Kb; ++kb, ++i) {
+          const int s = i % kStages;
+          const int buf = i % NB;
+          if (!mbar_wait(&tempty_bar[buf], ((i / NB) & 1) ^ 1, abort_flag) ||
+              !mbar_wait(&full_bar[s], (i / kStages) & 1, abort_flag)) {
+            fail();
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + buf * MP;
+#pragma unroll
+          for (int k = 0; k < kBlockK / 32; ++k) {
+            const uint64_t ad = smem_desc_sw128_kmajor(w_base + s * Cfg::kWBytes + k * 32);
+            const uint64_t bd = smem_desc_sw128_kmajor(x_base + s * Cfg::kXBytes + k * 32);
+            umma_e4m3(d_tmem, ad, bd, idesc, k > 0 ? 1u : 0u);
+          }
+          umma_commit(&empty_bar[s]);
+          umma_commit(&tfull_bar[buf]);
+        }
+      }
+      if (i > 0) {  // every issued MMA has finished before TMEM is released
+        umma_commit(drain_bar);
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(drain_bar, 0) && globaltimer_ns() - t0 < 200000000ull) {
+        }
+      }
+    }
+  } else if (warp < 4) {
+    // -------------------------------------------- promotion + epilogue
+    const int t = threadIdx.x;  // TMEM lane = column within the N tile
+    const uint32_t lane_base = uint32_t(warp * 32) << 16;
+    uint32_t gphase = 0;
+    bool ok = true;
+    auto group_sync = [&]() -> bool {
+      mbar_arrive(group_bar);
+      const bool r = mbar_wait(group_bar, gphase, abort_flag);
+      gphase ^= 1;
+      return r;
+    };
+    if (t == 0) {  // report entries that break the contract (once per launch)
+      for (int p = blockIdx.x; p < P; p += gridDim.x)
+        if (load_problem(tab, p, max_M).bad) raise_status(status, FP8GEMM_ERR_DEVICE_STATUS);
+    }
+    Walk w{tab, P, max_M};
+    int i = 0;
+    for (long long item = blockIdx.x; ok && w.seek(item); item += gridDim.x) {
+      const Prob q = w.cur;
+      const int tile = int(item - w.first);
+      float acc[MP];
+#pragma unroll
+      for (int j = 0; j < MP; ++j) acc[j] = 0.f;
+      for (int kb = 0; kb < q.Kb; ++kb, ++i) {
+        const int qq = kb % Cfg::kScaleKb;
+        if (qq == 0) {  // stage the next batch of scales
+          const int nkb = min(Cfg::kScaleKb, q.Kb - kb);
+          if (!group_sync()) { fail(); ok = false; break; }
+          for (int idx = t; idx < MP * nkb; idx += 128) {
+            const int j = idx / nkb, b = idx % nkb;
+            sa_s[b * MP + j] = j < q.M ? __ldg(q.sA + size_t(j) * q.Kb + kb + b) : 0.f;
+          }
+          if (t < nkb) sb_s[t] = __ldg(q.sB + size_t(tile) * q.Kb + kb + t);
+          if (!group_sync()) { fail(); ok = false; break; }
+        }
+        const int buf = i % NB;
+        if (!mbar_wait(&tfull_bar[buf], (i / NB) & 1, abort_flag)) {
+          fail();
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + lane_base + buf * MP;
+        const float sb = sb_s[qq];
+        const float* sa_row = sa_s + qq * MP;
+        if constexpr (MP == 16) {
+          uint32_t r[16];
+          tmem_ld_32x32b_x16(taddr, r);
+          tmem_ld_wait_tied16(r);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty_bar[buf]);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) acc[j] = fmaf(__uint_as_float(r[j]), sa_row[j] * sb, acc[j]);
+        } else {
+#pragma unroll
+          for (int cc = 0; cc < MP / 32; ++cc) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(taddr + cc * 32, r);
+            tmem_ld_wait_tied(r);
+            if (cc + 1 == MP / 32) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&tempty_bar[buf]);
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              acc[cc * 32 + j] =
+                  fmaf(__uint_as_float(r[j]), sa_row[cc * 32 + j] * sb, acc[cc * 32 + j]);
+          }
+        }
+      }
+      if (!ok) break;
+      const int n = tile * 128 + t;
+      if (n < q.N) {
+#pragma unroll
+        for (int j = 0; j < MP; ++j)
+          if (j < q.M) q.D[size_t(j) * q.N + n] = __float2bfloat16_rn(acc[j]);
+      }
+    }
+  }
+
+  __syncthreads();
+  if (warp == Cfg::kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+template <class Cfg>
+cudaError_t run(const LaunchCtx& c, const fp8gemm_problem* tab, int P, int max_M) {
+  static unsigned long long attr_done = 0;  // one bit per device
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!(attr_done >> (dev & 63) & 1ull)) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_table_kernel<Cfg>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(Cfg::kSmemBytes));
+    if (e != cudaSuccess) return e;
+    attr_done |= 1ull << (dev & 63);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(c.num_sms);
+  cfg.blockDim = dim3(Cfg::kThreads);
+  cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+  cfg.stream = c.stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_table_kernel<Cfg>, tab, P, max_M, c.status);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_table(const LaunchCtx& c, const fp8gemm_problem* tab, int P, int max_M) {
+  if (max_M <= 16) return run<TabCfg<16>>(c, tab, P, max_M);
+  if (max_M <= 32) return run<TabCfg<32>>(c, tab, P, max_M);
+  return run<TabCfg<64>>(c, tab, P, max_M);
+}
+
+}  // namespace fp8gemm

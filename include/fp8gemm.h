@@ -208,6 +208,45 @@ int fp8gemm_grouped_masked(const uint8_t* A, const float* sA, const uint8_t* B,
                            int E, int M_max, int N, int K, fp8gemm_stream_t stream);
 
 /*
+ * fp8gemm_grouped_table -- many independent dense problems in one launch,
+ * each described by an entry of a table in DEVICE memory, for batched decode
+ * requests ("bhfrc.com/news/60211" sections 4.2-4.3 and 6: shape data in
+ * device memory, so one captured CUDA graph can be replayed with new shapes).
+ * The launch depends only on num_problems and max_M; the table (pointers and
+ * sizes) is read on the device when the kernel runs, so it may be rewritten
+ * between replays of a graph that captured this call.
+ *
+ * Per entry p (e4m3 operands, the layouts and arithmetic of fp8gemm_dense):
+ *   A u8 [M, K], sA f32 [M, ceil(K/128)], B u8 [N, K],
+ *   sB f32 [ceil(N/128), ceil(K/128)], D bf16 [M, N] (written in full)
+ * with 0 <= M <= max_M <= 64, N >= 0, K > 0 and K % 16 == 0, A and B 16-byte
+ * aligned, sA and sB 4-byte, D 2-byte.  An entry with M = 0 or N = 0 is
+ * skipped.  An entry that breaks these rules is skipped and sets
+ * FP8GEMM_ERR_DEVICE_STATUS (read it with fp8gemm_get_device_status).
+ * Entries must not write overlapping D.
+ *
+ * Each (entry, 128-column tile) runs its whole K range on one CTA; there is
+ * no split-K across CTAs here, so a batch with few tiles in total leaves SMs
+ * idle (fp8gemm_dense splits K for a single problem).
+ *
+ *   problems  device array of num_problems entries, 8-byte aligned
+ * Host-side errors: FP8GEMM_ERR_SHAPE (num_problems < 0, max_M outside
+ * 1..64), FP8GEMM_ERR_NULL, FP8GEMM_ERR_ALIGN.
+ */
+typedef struct fp8gemm_problem {
+  const uint8_t* A;
+  const float* sA;
+  const uint8_t* B;
+  const float* sB;
+  void* D;
+  int M, N, K;
+  int reserved; /* set to 0 */
+} fp8gemm_problem;
+
+int fp8gemm_grouped_table(const fp8gemm_problem* problems, int num_problems, int max_M,
+                          fp8gemm_stream_t stream);
+
+/*
  * fp8gemm_dense_small_m_noalloc -- the same computation as fp8gemm_dense for
  * decode-sized M (1..64), for callers that must not have the library allocate
  * device memory: a server that reserves its whole memory budget up front and

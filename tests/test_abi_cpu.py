@@ -82,5 +82,24 @@ def test_host_validation_needs_no_gpu(lib):
     assert lib.fp8gemm_dense_fmt(None, good, 1, good, good, 0, good, 4, 256, 256, s) == b.ERR_NULL
     assert b.strerror(b.ERR_FORMAT).startswith("unknown FP8 format")
     assert lib.fp8_quant_128x128(good, None, good, 1, 8, 128, s) == b.ERR_NULL
+    assert lib.fp8gemm_grouped_table(good, -1, 16, s) == b.ERR_SHAPE
+    assert lib.fp8gemm_grouped_table(good, 4, 0, s) == b.ERR_SHAPE
+    assert lib.fp8gemm_grouped_table(good, 4, 65, s) == b.ERR_SHAPE
+    assert lib.fp8gemm_grouped_table(None, 4, 16, s) == b.ERR_NULL
+    assert lib.fp8gemm_grouped_table(P((1 << 20) + 4), 4, 16, s) == b.ERR_ALIGN
+    assert lib.fp8gemm_grouped_table(None, 0, 16, s) == b.OK
     assert lib.fp8gemm_get_device_status(s, None) == b.ERR_NULL
     assert isinstance(lib.fp8gemm_num_kernel_launches(), int)
+
+
+def test_problem_struct_layout():
+    """The binding's table entry has the C struct's size and field offsets
+    (5 pointers, then M, N, K, reserved)."""
+    from fp8_fine_grained_e4m3_gb300 import binding as b
+    assert ctypes.sizeof(b.Problem) == 56
+    assert [getattr(b.Problem, f).offset for f in ("A", "sA", "B", "sB", "D", "M", "N", "K")] == \
+        [0, 8, 16, 24, 32, 40, 44, 48]
+    hdr = open(os.path.join(ROOT, "include", "fp8gemm.h")).read()
+    body = hdr[hdr.index("typedef struct fp8gemm_problem"):hdr.index("} fp8gemm_problem;")]
+    assert re.findall(r"\*\s*(\w+);", body) == ["A", "sA", "B", "sB", "D"]
+    assert "int M, N, K;" in body and "int reserved;" in body

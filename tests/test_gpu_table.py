@@ -1,0 +1,106 @@
+"""fp8gemm_grouped_table: many decode-sized problems from a device-resident
+table, against the oracle; a captured CUDA graph replayed after the table was
+rewritten with other shapes and pointers; entries that are empty or break the
+contract."""
+
+import numpy as np
+import pytest
+
+from fp8_fine_grained_e4m3_gb300 import synthetic
+from tests.gpu_helpers import assert_close, dev, host, ogemm, oquant, quant_weights
+
+pytestmark = pytest.mark.gpu
+
+
+def _b():
+    from fp8_fine_grained_e4m3_gb300 import binding
+    return binding
+
+
+def _problem(M, N, K, seed):
+    import torch
+    X, W = synthetic.dense_operands(M, N, K, kind="decode", seed=seed)
+    A, sA = oquant.quant_1x128_fast(X)
+    B, sB = quant_weights(W)
+    ref = ogemm.gemm_dense(A, sA, B, sB)
+    D = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    return (dev(A), dev(sA), dev(B), dev(sB), D), ref
+
+
+SHAPES = [(1, 2048, 7168), (5, 300, 400), (16, 7168, 2048), (33, 777, 1024), (64, 128, 256),
+          (7, 1000, 272), (64, 2048, 2048), (2, 129, 4096)]
+
+
+@pytest.mark.parametrize("max_M,shapes", [
+    (64, SHAPES),                                            # 64-wide kernel, mixed shapes
+    (16, [(1, 2048, 7168), (5, 300, 400), (16, 640, 1024)]),  # 16-wide kernel
+    (32, [(20, 1536, 7168), (32, 256, 144)]),                 # 32-wide kernel, partial K block
+])
+def test_table_matches_oracle(max_M, shapes):
+    b = _b()
+    probs, refs = zip(*[_problem(M, N, K, seed=i + M) for i, (M, N, K) in enumerate(shapes)])
+    table = b.problem_table(probs)
+    b.fp8gemm_grouped_table(table, len(probs), max_M)
+    for (_, _, _, _, D), ref, shp in zip(probs, refs, shapes):
+        assert_close(host(D), ref, f"table problem {shp}")
+    assert b.fp8gemm_get_device_status() == b.OK
+
+
+def test_graph_replay_with_rewritten_table():
+    """The launch is captured once; between replays the table is rewritten
+    in place with problems of other sizes and buffers."""
+    import torch
+    b = _b()
+    first = [_problem(M, N, K, seed=40 + i) for i, (M, N, K) in enumerate([(4, 640, 2048), (9, 2048, 512)])]
+    second = [_problem(M, N, K, seed=50 + i) for i, (M, N, K) in
+              enumerate([(16, 384, 1024), (1, 7168, 256), (12, 200, 400)])]
+    P = 3
+    table = torch.zeros(P * 56, dtype=torch.uint8, device="cuda")
+    # the first set padded with an empty entry (M = 0) to the captured count
+    empty = (first[0][0][0][:0], first[0][0][1][:0], first[0][0][2], first[0][0][3],
+             first[0][0][4][:0])
+    b.problem_table([p for p, _ in first] + [empty], out=table)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        b.fp8gemm_grouped_table(table, P, 16)  # warm-up outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        b.fp8gemm_grouped_table(table, P, 16)
+    for (probs, _) in first:
+        probs[4].fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    for (probs, ref) in first:
+        assert_close(host(probs[4]), ref, "replay 1")
+    b.problem_table([p for p, _ in second], out=table)
+    g.replay()
+    torch.cuda.synchronize()
+    for (probs, ref) in second:
+        assert_close(host(probs[4]), ref, "replay 2 (rewritten table)")
+    assert b.fp8gemm_get_device_status() == b.OK
+
+
+def test_bad_and_empty_entries():
+    import torch
+    b = _b()
+    good, ref = _problem(8, 512, 1024, seed=7)
+    other, ref2 = _problem(3, 256, 256, seed=8)
+    import ctypes
+    arr = (b.Problem * 4)()
+    for e, (A, sA, B, sB, D) in zip(arr, [good, other, good, good]):
+        e.A, e.sA, e.B, e.sB, e.D = (A.data_ptr(), sA.data_ptr(), B.data_ptr(), sB.data_ptr(),
+                                     D.data_ptr())
+        e.M, e.K = A.shape
+        e.N = B.shape[0]
+    arr[2].M = 65            # beyond max_M: skipped, status raised
+    arr[3].A = arr[3].A + 4  # misaligned A: skipped, status raised
+    bad_D = torch.full((8, 512), 7.0, dtype=torch.bfloat16, device="cuda")
+    arr[2].D = arr[3].D = bad_D.data_ptr()
+    table = torch.frombuffer(bytearray(bytes(arr)), dtype=torch.uint8).cuda()
+    b.fp8gemm_grouped_table(table, 4, 64)
+    assert b.fp8gemm_get_device_status() == b.ERR_DEVICE_STATUS
+    assert_close(host(good[4]), ref, "good entry beside bad ones")
+    assert_close(host(other[4]), ref2, "second good entry")
+    assert bool((bad_D == 7.0).all())  # skipped entries write nothing
+    assert b.fp8gemm_get_device_status() == b.OK  # the read cleared it
