@@ -616,6 +616,17 @@ def run_kernel_case(name, reps):
         else:
             del X, W
             fn = lambda: b.fp8gemm_dense(A8, sA, B8, sB, D=D)  # noqa: E731
+    elif name == "table":
+        E, M_max, N, K = 16, 16, 4096, 7168
+        mm = (synthetic.masked_counts(E, M_max - 1, seed=3) + 1).astype("int32")
+        X = synthetic.masked_activations_device(E, M_max, K, seed=3, device=dev)
+        A8, sA = b.fp8_quant_1x128(X)
+        del X
+        B8, sB = b.fp8_quant_128x128(synthetic.expert_weights_device(E, N, K, seed=4, device=dev))
+        D = torch.empty((E, M_max, N), dtype=torch.bfloat16, device=dev)
+        table = b.problem_table([(A8[e, :mm[e]], sA[e, :mm[e]], B8[e], sB[e], D[e, :mm[e]])
+                                 for e in range(E)])
+        fn = lambda: b.fp8gemm_grouped_table(table, E, M_max)  # noqa: E731
     elif name in ("contiguous", "masked"):
         if name == "contiguous":
             E, N, K = 32, 4096, 7168

@@ -43,6 +43,9 @@ SIGNATURES = [
     ("fp8_quant_128x128_fmt", _I, [_P, _P, _P, _I, _I, _I, _I, _P]),
     ("fp8gemm_dense_fmt", _I, [_P, _P, _I, _P, _P, _I, _P, _I, _I, _I, _P]),
     ("fp8gemm_grouped_table", _I, [_P, _I, _I, _P]),
+    ("fp8gemm_grouped_contiguous_fmt", _I,
+     [_P, _P, _I, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P]),
+    ("fp8gemm_grouped_masked_fmt", _I, [_P, _P, _I, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P]),
     ("fp8gemm_dense_quant_a", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
     ("fp8gemm_grouped_contiguous", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     ("fp8gemm_grouped_masked", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
@@ -328,6 +331,36 @@ def fp8gemm_grouped_masked(A, sA, B, sB, masked_m, D=None, stream=None):
         _ptr(A), _ptr(_f32(sA, "sA")), _ptr(B), _ptr(_f32(sB, "sB")),
         _ptr(_i32(masked_m, "masked_m")), _ptr(_dev(D, "D")), E, M_max, N, K,
         _stream(stream)), "fp8gemm_grouped_masked")
+    return D
+
+
+def fp8gemm_grouped_contiguous_fmt(A, sA, a_fmt, B, sB, b_fmt, m_indices, D=None, stream=None):
+    """fp8gemm_grouped_contiguous with operand formats ("e4m3" / "e5m2")."""
+    torch = _torch()
+    A, B = _u8(A, "A"), _u8(B, "B")
+    M_pad, K = A.shape
+    E, N = B.shape[0], B.shape[1]
+    if D is None:
+        D = torch.empty((M_pad, N), dtype=torch.bfloat16, device=A.device)
+    _check(lib().fp8gemm_grouped_contiguous_fmt(
+        _ptr(A), _ptr(_f32(sA, "sA")), _fmt(a_fmt), _ptr(B), _ptr(_f32(sB, "sB")), _fmt(b_fmt),
+        _ptr(_i32(m_indices, "m_indices")), _ptr(_dev(D, "D")), M_pad, N, K, E,
+        _stream(stream)), "fp8gemm_grouped_contiguous_fmt")
+    return D
+
+
+def fp8gemm_grouped_masked_fmt(A, sA, a_fmt, B, sB, b_fmt, masked_m, D=None, stream=None):
+    """fp8gemm_grouped_masked with operand formats ("e4m3" / "e5m2")."""
+    torch = _torch()
+    A, B = _u8(A, "A"), _u8(B, "B")
+    E, M_max, K = A.shape
+    N = B.shape[1]
+    if D is None:
+        D = torch.empty((E, M_max, N), dtype=torch.bfloat16, device=A.device)
+    _check(lib().fp8gemm_grouped_masked_fmt(
+        _ptr(A), _ptr(_f32(sA, "sA")), _fmt(a_fmt), _ptr(B), _ptr(_f32(sB, "sB")), _fmt(b_fmt),
+        _ptr(_i32(masked_m, "masked_m")), _ptr(_dev(D, "D")), E, M_max, N, K,
+        _stream(stream)), "fp8gemm_grouped_masked_fmt")
     return D
 
 

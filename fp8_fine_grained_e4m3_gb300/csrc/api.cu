@@ -278,12 +278,16 @@ int fp8gemm_grouped_table(const fp8gemm_problem* problems, int num_problems, int
   return finish(launch_gemm_table(c, problems, num_problems, max_M), 1);
 }
 
-int fp8gemm_grouped_contiguous(const uint8_t* A, const float* sA, const uint8_t* B,
-                               const float* sB, const int32_t* m_indices, void* D, int M_pad,
-                               int N, int K, int E, fp8gemm_stream_t stream) {
+static bool valid_fmt(int f) { return f == FP8GEMM_FMT_E4M3 || f == FP8GEMM_FMT_E5M2; }
+
+int fp8gemm_grouped_contiguous_fmt(const uint8_t* A, const float* sA, int a_fmt,
+                                   const uint8_t* B, const float* sB, int b_fmt,
+                                   const int32_t* m_indices, void* D, int M_pad, int N, int K,
+                                   int E, fp8gemm_stream_t stream) {
   if (int r = check_common(M_pad, N, K)) return r;
   if (E < 0 || M_pad % kBlockM != 0) return FP8GEMM_ERR_SHAPE;
   if ((long long)E * N > 0x7fffffffLL) return FP8GEMM_ERR_SHAPE;
+  if (!valid_fmt(a_fmt) || !valid_fmt(b_fmt)) return FP8GEMM_ERR_FORMAT;
   if (M_pad == 0 || N == 0 || E == 0) return FP8GEMM_OK;
   if (!A || !sA || !B || !sB || !m_indices || !D) return FP8GEMM_ERR_NULL;
   if (!aligned16(A) || !aligned16(sA) || !aligned16(B) || !aligned16(sB) ||
@@ -293,16 +297,26 @@ int fp8gemm_grouped_contiguous(const uint8_t* A, const float* sA, const uint8_t*
   if (int r = ctx_for(stream, &c)) return r;
   GemmArgs a{GemmMode::kContiguous, A, sA, B, sB, m_indices, static_cast<__nv_bfloat16*>(D),
              M_pad, N, K, E};
+  a.a_fmt = a_fmt;
+  a.b_fmt = b_fmt;
   return finish(launch_gemm_tc(c, a), 1);
 }
 
-int fp8gemm_grouped_masked(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
-                           const int32_t* masked_m, void* D, int E, int M_max, int N, int K,
-                           fp8gemm_stream_t stream) {
+int fp8gemm_grouped_contiguous(const uint8_t* A, const float* sA, const uint8_t* B,
+                               const float* sB, const int32_t* m_indices, void* D, int M_pad,
+                               int N, int K, int E, fp8gemm_stream_t stream) {
+  return fp8gemm_grouped_contiguous_fmt(A, sA, FP8GEMM_FMT_E4M3, B, sB, FP8GEMM_FMT_E4M3,
+                                        m_indices, D, M_pad, N, K, E, stream);
+}
+
+int fp8gemm_grouped_masked_fmt(const uint8_t* A, const float* sA, int a_fmt, const uint8_t* B,
+                               const float* sB, int b_fmt, const int32_t* masked_m, void* D,
+                               int E, int M_max, int N, int K, fp8gemm_stream_t stream) {
   if (int r = check_common(M_max, N, K)) return r;
   if (E < 0) return FP8GEMM_ERR_SHAPE;
   if ((long long)E * M_max > 0x7fffffffLL || (long long)E * N > 0x7fffffffLL)
     return FP8GEMM_ERR_SHAPE;
+  if (!valid_fmt(a_fmt) || !valid_fmt(b_fmt)) return FP8GEMM_ERR_FORMAT;
   if (M_max == 0 || N == 0 || E == 0) return FP8GEMM_OK;
   if (!A || !sA || !B || !sB || !masked_m || !D) return FP8GEMM_ERR_NULL;
   if (!aligned16(A) || !aligned16(sA) || !aligned16(B) || !aligned16(sB) ||
@@ -312,7 +326,16 @@ int fp8gemm_grouped_masked(const uint8_t* A, const float* sA, const uint8_t* B, 
   if (int r = ctx_for(stream, &c)) return r;
   GemmArgs a{GemmMode::kMasked, A, sA, B, sB, masked_m, static_cast<__nv_bfloat16*>(D),
              M_max, N, K, E};
+  a.a_fmt = a_fmt;
+  a.b_fmt = b_fmt;
   return finish(launch_gemm_tc(c, a), 1);
+}
+
+int fp8gemm_grouped_masked(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                           const int32_t* masked_m, void* D, int E, int M_max, int N, int K,
+                           fp8gemm_stream_t stream) {
+  return fp8gemm_grouped_masked_fmt(A, sA, FP8GEMM_FMT_E4M3, B, sB, FP8GEMM_FMT_E4M3, masked_m,
+                                    D, E, M_max, N, K, stream);
 }
 
 int fp8gemm_get_device_status(fp8gemm_stream_t stream, int* out) {

@@ -208,6 +208,19 @@ int fp8gemm_grouped_masked(const uint8_t* A, const float* sA, const uint8_t* B,
                            int E, int M_max, int N, int K, fp8gemm_stream_t stream);
 
 /*
+ * fp8gemm_grouped_contiguous_fmt / fp8gemm_grouped_masked_fmt -- the two
+ * grouped forms with each operand's format given (FP8GEMM_FMT_*), as
+ * fp8gemm_dense_fmt does for the dense form; all else as the e4m3 calls.
+ */
+int fp8gemm_grouped_contiguous_fmt(const uint8_t* A, const float* sA, int a_fmt,
+                                   const uint8_t* B, const float* sB, int b_fmt,
+                                   const int32_t* m_indices, void* D, int M_pad, int N, int K,
+                                   int E, fp8gemm_stream_t stream);
+int fp8gemm_grouped_masked_fmt(const uint8_t* A, const float* sA, int a_fmt, const uint8_t* B,
+                               const float* sB, int b_fmt, const int32_t* masked_m, void* D,
+                               int E, int M_max, int N, int K, fp8gemm_stream_t stream);
+
+/*
  * fp8gemm_grouped_table -- many independent dense problems in one launch,
  * each described by an entry of a table in DEVICE memory, for batched decode
  * requests ("bhfrc.com/news/60211" sections 4.2-4.3 and 6: shape data in

@@ -91,7 +91,7 @@ def gemm_dense_at(A, sA, B, sB, rows, cols, a_fmt="e4m3", b_fmt="e4m3") -> np.nd
                          _decoder(b_fmt)(np.asarray(B)[cols]), sB[cols // BLOCK])
 
 
-def gemm_contiguous(A, sA, B, sB, m_indices) -> np.ndarray:
+def gemm_contiguous(A, sA, B, sB, m_indices, a_fmt="e4m3", b_fmt="e4m3") -> np.ndarray:
     """A u8 [M_pad, K], sA [M_pad, Kb], B u8 [E, N, K], sB [E, Nb, Kb],
     m_indices i32 [M_pad] -> f64 [M_pad, N]; padding rows (index -1) are NaN."""
     A = np.asarray(A, dtype=np.uint8)
@@ -101,11 +101,11 @@ def gemm_contiguous(A, sA, B, sB, m_indices) -> np.ndarray:
     for e in range(E):
         r = np.nonzero(m_indices == e)[0]
         if r.size:
-            D[r] = gemm_dense(A[r], np.asarray(sA)[r], B[e], sB[e])
+            D[r] = gemm_dense(A[r], np.asarray(sA)[r], B[e], sB[e], a_fmt, b_fmt)
     return D
 
 
-def gemm_masked(A, sA, B, sB, masked_m) -> np.ndarray:
+def gemm_masked(A, sA, B, sB, masked_m, a_fmt="e4m3", b_fmt="e4m3") -> np.ndarray:
     """A u8 [E, M_max, K], sA [E, M_max, Kb], B u8 [E, N, K], sB [E, Nb, Kb],
     masked_m i32 [E] -> f64 [E, M_max, N]; rows >= masked_m[e] are NaN."""
     E, M_max, K = A.shape
@@ -114,7 +114,7 @@ def gemm_masked(A, sA, B, sB, masked_m) -> np.ndarray:
     for e in range(E):
         m = int(masked_m[e])
         if m > 0:
-            D[e, :m] = gemm_dense(A[e, :m], sA[e, :m], B[e], sB[e])
+            D[e, :m] = gemm_dense(A[e, :m], sA[e, :m], B[e], sB[e], a_fmt, b_fmt)
     return D
 
 

@@ -81,6 +81,10 @@ def test_host_validation_needs_no_gpu(lib):
     assert lib.fp8gemm_dense_fmt(good, good, 1, good, good, 1, good, 4, 256, 136, s) == b.ERR_SHAPE
     assert lib.fp8gemm_dense_fmt(None, good, 1, good, good, 0, good, 4, 256, 256, s) == b.ERR_NULL
     assert b.strerror(b.ERR_FORMAT).startswith("unknown FP8 format")
+    assert lib.fp8gemm_grouped_contiguous_fmt(good, good, 0, good, good, 3, good, good,
+                                              128, 256, 256, 2, s) == b.ERR_FORMAT
+    assert lib.fp8gemm_grouped_masked_fmt(good, good, 9, good, good, 0, good, good,
+                                          2, 128, 256, 256, s) == b.ERR_FORMAT
     assert lib.fp8_quant_128x128(good, None, good, 1, 8, 128, s) == b.ERR_NULL
     assert lib.fp8gemm_grouped_table(good, -1, 16, s) == b.ERR_SHAPE
     assert lib.fp8gemm_grouped_table(good, 4, 0, s) == b.ERR_SHAPE

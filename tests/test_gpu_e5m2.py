@@ -71,3 +71,34 @@ def test_e4m3_through_fmt_call_is_the_plain_call():
     d1 = host(b.fp8gemm_dense(tA, tsA, tB, tsB))
     d2 = host(b.fp8gemm_dense_fmt(tA, tsA, "e4m3", tB, tsB, "e4m3"))
     assert np.array_equal(d1, d2)
+
+
+@pytest.mark.parametrize("a_fmt,b_fmt", [("e5m2", "e4m3"), ("e4m3", "e5m2")])
+def test_grouped_mixed_formats(a_fmt, b_fmt):
+    """Contiguous and masked grouped forms with e5m2 operands."""
+    import torch
+    b = _b()
+    E, N, K = 3, 384, 512
+    X, W, lay = synthetic.contiguous_operands(E, 300, N, K, seed=9)
+    A, sA = oq.quant_1x128_fast(X, fmt=a_fmt)
+    Bq = [_q128(W[e], b_fmt) for e in range(E)]
+    B = np.stack([q for q, _ in Bq])
+    sB = np.stack([s_ for _, s_ in Bq])
+    got = host(b.fp8gemm_grouped_contiguous_fmt(dev(A), dev(sA), a_fmt, dev(B), dev(sB), b_fmt,
+                                                dev(lay.m_indices.astype(np.int32))))
+    ref = ogemm.gemm_contiguous(A, sA, B, sB, lay.m_indices, a_fmt, b_fmt)
+    assert_close(got, ref, f"contiguous {a_fmt} x {b_fmt}")
+
+    Xm, Wm, mm = synthetic.masked_operands(E, 160, N, K, seed=10,
+                                           masked_m=np.array([160, 0, 37], np.int32))
+    Am, sAm = oq.quant_1x128_fast(Xm.reshape(-1, K), fmt=a_fmt)
+    Am, sAm = Am.reshape(E, 160, K), sAm.reshape(E, 160, -1)
+    Bq = [_q128(Wm[e], b_fmt) for e in range(E)]
+    Bm = np.stack([q for q, _ in Bq])
+    sBm = np.stack([s_ for _, s_ in Bq])
+    D = torch.zeros((E, 160, N), dtype=torch.bfloat16, device="cuda")
+    b.fp8gemm_grouped_masked_fmt(dev(Am), dev(sAm), a_fmt, dev(Bm), dev(sBm), b_fmt,
+                                 dev(mm), D=D)
+    ref = ogemm.gemm_masked(Am, sAm, Bm, sBm, mm, a_fmt, b_fmt)
+    assert_close(host(D), ref, f"masked {a_fmt} x {b_fmt}")
+    assert b.fp8gemm_get_device_status() == b.OK
