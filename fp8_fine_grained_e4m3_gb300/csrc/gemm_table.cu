@@ -35,6 +35,8 @@ template <int MP_>
 struct TabCfg {
   static constexpr int MP = MP_;
   static constexpr int kStages = 6;
+  // two CTAs per SM where they fit (MP = 16): twice the copies in flight
+  static constexpr int kCtasPerSm = MP == 16 ? 2 : 1;
   static constexpr int kThreads = 288;
   static constexpr int kLoadWarp = 4;  // warps 4-7 load
   static constexpr int kLoadWarps = 4;
@@ -50,6 +52,7 @@ struct TabCfg {
       1024 + size_t(kStages) * (kWBytes + kXBytes) + kAuxBytes;
   static_assert((2 * kStages + 2 * kTmemBufs + 4) * 8 + 16 <= kBarBytes, "barrier area");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+  static_assert(kCtasPerSm == 1 || kSmemBytes <= 113 * 1024, "two CTAs per SM");
 };
 
 // A problem as the kernels use it: its table entry, or an empty problem if
@@ -113,7 +116,7 @@ struct Walk {
 };
 
 template <class Cfg>
-__global__ void __launch_bounds__(Cfg::kThreads, 1)
+__global__ void __launch_bounds__(Cfg::kThreads, Cfg::kCtasPerSm)
     gemm_table_kernel(const fp8gemm_problem* __restrict__ tab, int P, int max_M, int* status) {
   constexpr int MP = Cfg::MP;
   constexpr int kStages = Cfg::kStages;
@@ -349,7 +352,7 @@ cudaError_t run(const LaunchCtx& c, const fp8gemm_problem* tab, int P, int max_M
     attr_done |= 1ull << (dev & 63);
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(c.num_sms);
+  cfg.gridDim = dim3(c.num_sms * Cfg::kCtasPerSm);
   cfg.blockDim = dim3(Cfg::kThreads);
   cfg.dynamicSmemBytes = Cfg::kSmemBytes;
   cfg.stream = c.stream;
