@@ -110,7 +110,9 @@ int workspace_for(cudaStream_t s, size_t bytes, void** out, int slot = kWsSplitK
   }
   void* p = nullptr;
   if (cudaMalloc(&p, bytes) != cudaSuccess) return FP8GEMM_ERR_LAUNCH;
-  if (cudaMemset(p, 0, bytes) != cudaSuccess) {
+  // zeroed on the stream that will use it: a plain cudaMemset runs on the
+  // legacy default stream, which a non-blocking stream does not wait for
+  if (cudaMemsetAsync(p, 0, bytes, s) != cudaSuccess) {
     cudaFree(p);
     return FP8GEMM_ERR_LAUNCH;
   }

@@ -43,12 +43,14 @@
  *    FP8GEMM_ERR_TIMEOUT in a per-device status word, skips the offending
  *    tile and finishes.  Read it with fp8gemm_get_device_status().
  *  - Inputs and outputs must not overlap.
- *  - The dense path for M <= 64 splits K across CTAs and reduces partial sums
- *    through a per-(device, stream) workspace that the library allocates with
- *    cudaMalloc on the first such call on that stream (about 10 MB, kept until
- *    process exit).  That first call must therefore not happen during CUDA
- *    graph capture.  The reduction order is fixed, so results are
- *    deterministic.
+ *  - The dense path for M <= 64 may split K across CTAs and reduce partial
+ *    sums through a per-(device, stream) workspace that the library allocates
+ *    with cudaMalloc on the first such call on that stream (about 10 MB, kept
+ *    until process exit) and zeroes on that stream; fp8gemm_dense_quant_a at
+ *    M > 64 without Q/sA keeps its quantised A in a second per-stream buffer.
+ *    Such a first call must therefore not happen during CUDA graph capture.
+ *    Calls on different streams never share a workspace.  The reduction
+ *    order is fixed, so results are deterministic.
  */
 #ifndef FP8GEMM_H
 #define FP8GEMM_H

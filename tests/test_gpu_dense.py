@@ -111,3 +111,42 @@ def test_decode_chain_without_host_sync(M, N, K):
     for got, ref in zip(outs, refs):
         assert_close(host(got), ref, f"chained decode {M}x{N}x{K}")
     assert b.fp8gemm_get_device_status() == b.OK
+
+
+def test_two_streams_with_library_workspaces():
+    """Calls that use the library's per-stream workspaces (split-K partials
+    and counters of the decode path; the quantised A of the FP32-activation
+    call) issued on two streams with no ordering between them: each stream
+    has its own workspace, so the results are those of running them alone."""
+    import torch
+    b = _b()
+    cases = []
+    for seed, (M, N, K) in enumerate([(17, 128, 16384), (33, 1000, 1280), (5, 128, 131072)]):
+        A, sA, B, sB = quantised_dense(M, N, K, "decode", seed=60 + seed)
+        cases.append(((dev(A), dev(sA), dev(B), dev(sB)), ogemm.gemm_dense(A, sA, B, sB)))
+    X = synthetic_ops(200, 2304, 1024)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    outs = []
+    torch.cuda.synchronize()
+    for rep in range(3):
+        for i, ((tA, tsA, tB, tsB), _) in enumerate(cases):
+            s = s1 if (i + rep) % 2 == 0 else s2
+            with torch.cuda.stream(s):
+                outs.append((i, b.fp8gemm_dense(tA, tsA, tB, tsB)))
+        with torch.cuda.stream(s2 if rep % 2 == 0 else s1):
+            outs.append((-1, b.fp8gemm_dense_quant_a(X[0], X[1], X[2])))
+    torch.cuda.synchronize()
+    for i, D in outs:
+        ref = cases[i][1] if i >= 0 else X[3]
+        assert_close(host(D), ref, f"two streams, case {i}")
+    assert b.fp8gemm_get_device_status() == b.OK
+
+
+def synthetic_ops(M, N, K):
+    """FP32 activations, oracle-quantised weights and the reference result of
+    fp8gemm_dense_quant_a for them."""
+    from fp8_fine_grained_e4m3_gb300 import synthetic
+    Xf, Wf = synthetic.dense_operands(M, N, K, kind="decode", seed=70)
+    Ao, sAo = oquant.quant_1x128_fast(Xf)
+    Bo, sBo = oquant.quant_128x128_fast(Wf)
+    return dev(Xf), dev(Bo), dev(sBo), ogemm.gemm_dense(Ao, sAo, Bo, sBo)
