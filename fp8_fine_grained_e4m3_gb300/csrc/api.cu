@@ -16,6 +16,12 @@ namespace fp8gemm {
 
 // Per-device status word (one instance per device the library is loaded on).
 __device__ int g_device_status = 0;
+// Where exchange_status leaves the word it took.
+__device__ int g_status_taken = 0;
+
+// Reads and clears the status word in one atomic step, so that a condition a
+// kernel on another stream raises meanwhile is either returned or kept.
+__global__ void exchange_status(int* status) { g_status_taken = atomicExch(status, 0); }
 
 namespace {
 
@@ -344,12 +350,13 @@ int fp8gemm_get_device_status(fp8gemm_stream_t stream, int* out) {
   if (!out) return FP8GEMM_ERR_NULL;
   DeviceInfo d;
   if (int r = device_info(&d)) return r;
-  if (cudaStreamSynchronize(stream) != cudaSuccess) return FP8GEMM_ERR_LAUNCH;
+  exchange_status<<<1, 1, 0, stream>>>(d.status);  // after every earlier kernel on stream
+  if (cudaGetLastError() != cudaSuccess) return FP8GEMM_ERR_LAUNCH;
+  g_launches += 1;
   int v = 0;
-  if (cudaMemcpy(&v, d.status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
-    return FP8GEMM_ERR_LAUNCH;
-  const int zero = 0;
-  if (cudaMemcpy(d.status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+  if (cudaMemcpyFromSymbolAsync(&v, g_status_taken, sizeof(int), 0, cudaMemcpyDeviceToHost,
+                                stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
     return FP8GEMM_ERR_LAUNCH;
   *out = v;
   return FP8GEMM_OK;

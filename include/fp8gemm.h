@@ -293,10 +293,14 @@ int fp8gemm_dense_small_m_noalloc(const uint8_t* A, const float* sA, const uint8
                                   fp8gemm_stream_t stream);
 
 /*
- * fp8gemm_get_device_status -- synchronise `stream`, then read and clear the
- * current device's status word: *out = FP8GEMM_OK, FP8GEMM_ERR_DEVICE_STATUS
- * or FP8GEMM_ERR_TIMEOUT.  Returns FP8GEMM_OK, or FP8GEMM_ERR_NULL /
- * FP8GEMM_ERR_LAUNCH if `out` is NULL or the CUDA calls fail.
+ * fp8gemm_get_device_status -- after every kernel enqueued on `stream` so
+ * far, read and clear the current device's status word in one atomic step
+ * (a one-thread kernel on `stream`), then synchronise `stream`:
+ * *out = FP8GEMM_OK, FP8GEMM_ERR_DEVICE_STATUS or FP8GEMM_ERR_TIMEOUT.  A
+ * condition raised meanwhile by a kernel on another stream is either
+ * returned here or left for the next read.  Returns FP8GEMM_OK, or
+ * FP8GEMM_ERR_NULL / FP8GEMM_ERR_LAUNCH if `out` is NULL or the CUDA calls
+ * fail.
  */
 int fp8gemm_get_device_status(fp8gemm_stream_t stream, int* out);
 
