@@ -387,6 +387,15 @@ def measure_configs(peaks, dev):
     ms = time_launch(lambda: b.fp8gemm_dense(A8, sA, B8, sB, D=D), flush)
     res["dense_128x256x512"] = _roof(2 * 128 * 256 * 512, gemm_bytes(128, 256, 512), ms, peaks)
 
+    # a few hundred rows: every tile fits in one wave, so each tile's K blocks
+    # are shared by a cluster of CTAs (split instance)
+    for (M, N, K) in ((128, 4096, 7168), (384, 4096, 7168)):
+        A8, sA, B8, sB, D = dense_case(M, N, K, "prefill", M)
+        ms = time_launch(lambda: b.fp8gemm_dense(A8, sA, B8, sB, D=D), flush)
+        r = _roof(2 * M * N * K, gemm_bytes(M, N, K), ms, peaks)
+        r["note"] = "tiles split along K over thread-block clusters"
+        res[f"dense_split_{M}x{N}x{K}"] = r
+
     for M in (1, 16, 64):
         for (N, K) in ((7168, 2048), (2048, 7168)):
             # 24 weight copies (> 2x L2 in total) used in turn, launched back to
@@ -626,7 +635,7 @@ def run_kernel_case(name, reps):
     dev = torch.device("cuda", 0)
     shapes = {"gemm_prefill": (4096, 7168, 16384), "gemm_square": (4096, 4096, 4096),
               "gemm_decode64": (64, 7168, 2048), "gemm_decode1": (1, 7168, 2048),
-              "quant": (4096, 8, 16384)}
+              "gemm_split": (128, 4096, 7168), "quant": (4096, 8, 16384)}
     if name in shapes:
         M, N, K = shapes[name]
         X, W = synthetic.dense_operands_device(M, N, K, kind="prefill", seed=0, device=dev)

@@ -129,6 +129,14 @@ int workspace_for(cudaStream_t s, size_t bytes, void** out, int slot = kWsSplitK
 
 constexpr int kSmallM = 64;  // dense calls with M <= this use the swap-AB stream-K kernel
 
+// The persistent tensor-core GEMM (its launch count is 0 for an empty
+// problem, else 1).
+int run_gemm_tc(const LaunchCtx& c, const GemmArgs& a) {
+  int launches = 0;
+  const cudaError_t e = launch_gemm_tc(c, a, &launches);
+  return finish(e, launches);
+}
+
 }  // namespace
 
 bool make_tmap_u8_sw128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
@@ -241,7 +249,7 @@ int fp8gemm_dense_fmt(const uint8_t* A, const float* sA, int a_fmt, const uint8_
     if (int r = workspace_for(stream, bytes, &ws)) return r;
     return finish(launch_gemm_small_m_any(c, a, ws, bytes), 1);
   }
-  return finish(launch_gemm_tc(c, a), 1);
+  return run_gemm_tc(c, a);
 }
 
 int fp8gemm_dense(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB, void* D,
@@ -307,7 +315,7 @@ int fp8gemm_grouped_contiguous_fmt(const uint8_t* A, const float* sA, int a_fmt,
              M_pad, N, K, E};
   a.a_fmt = a_fmt;
   a.b_fmt = b_fmt;
-  return finish(launch_gemm_tc(c, a), 1);
+  return run_gemm_tc(c, a);
 }
 
 int fp8gemm_grouped_contiguous(const uint8_t* A, const float* sA, const uint8_t* B,
@@ -336,7 +344,7 @@ int fp8gemm_grouped_masked_fmt(const uint8_t* A, const float* sA, int a_fmt, con
              M_max, N, K, E};
   a.a_fmt = a_fmt;
   a.b_fmt = b_fmt;
-  return finish(launch_gemm_tc(c, a), 1);
+  return run_gemm_tc(c, a);
 }
 
 int fp8gemm_grouped_masked(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,

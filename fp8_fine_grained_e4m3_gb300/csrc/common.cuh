@@ -53,9 +53,15 @@ struct GemmArgs {
   int E;      // experts (1 for dense)
   int a_fmt = FP8GEMM_FMT_E4M3;  // operand formats (tensor-core type codes: e4m3 0, e5m2 1)
   int b_fmt = FP8GEMM_FMT_E4M3;
+  // Parts per tile along K (persistent tensor-core GEMM, split instance:
+  // one cluster of `split` CTAs per tile).  1: whole tiles.
+  int split = 1;
 };
 
-cudaError_t launch_gemm_tc(const LaunchCtx& c, const GemmArgs& a);
+constexpr int kMaxSplit = 8;  // parts (cluster CTAs) per split tile, at most
+
+// The persistent tensor-core GEMM (one launch; the count goes to *launches).
+cudaError_t launch_gemm_tc(const LaunchCtx& c, const GemmArgs& a, int* launches);
 cudaError_t launch_gemm_small_m(const LaunchCtx& c, const GemmArgs& a, void* workspace,
                                 size_t workspace_bytes);
 size_t small_m_workspace_bytes(int num_sms, int N);

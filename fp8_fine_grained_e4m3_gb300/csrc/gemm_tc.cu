@@ -30,6 +30,17 @@
 // loads the next block while the matrix instruction consumes the current
 // one, with mbarriers between them.)
 //
+// Split tiles: when every tile fits in one wave (fewer tiles than SMs, as for
+// a few hundred rows), most SMs would idle.  A second instance of the kernel
+// (kTail) then gives each tile a cluster of `split` CTAs, CTA r contracting
+// the r-th share of the K blocks.  Each CTA stages its FP32 partial in its
+// own shared memory (the idle operand ring); after a cluster barrier CTA r
+// sums row band r of the tile over the cluster's CTAs, in rank order, through
+// distributed shared memory and writes it to D ("news.rkmt.cn/news/5092"
+// section 3.2: size the work to the SM count).  Splitting only the last wave
+// of a longer run was slower: that wave's parts start cold behind the other
+// waves.
+//
 // Tile order: grouped rasterisation (16 M blocks share each sweep over N) so
 // concurrently running CTAs reuse A and B tiles through L2 ("news.rkmt.cn/
 // news/5092" section 3.2: size the work to the SM count).  The masked form
@@ -163,6 +174,17 @@ struct Scheduler {
   }
 };
 
+// Split tiles: a CTA's FP32 partial of its tile, staged row-major in its own
+// shared memory (the operand ring, idle once its last K block is contracted).
+// Rows are padded by 4 floats: the 8 lanes of each quarter-warp store a float4
+// of 8 consecutive rows into 8 distinct bank groups.
+template <class Cfg>
+struct Stage {
+  static constexpr int kPitch = Cfg::BN + 4;  // floats per staged row
+  static constexpr size_t kBytes = size_t(kBlockM) * kPitch * 4;
+  static_assert(kBytes <= size_t(Cfg::kStages) * Cfg::kStageBytes, "staging fits the ring");
+};
+
 // Bounded wait on an mbarrier whose phases may already be complete, with no
 // abort check: used only to let in-flight async copies land before exit.
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
@@ -172,7 +194,10 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
-template <class Cfg>
+// kTail = false: whole tiles, persistent over the CTAs.  kTail = true (all
+// tiles fit in one wave): cluster c of args.split CTAs computes tile c, CTA
+// rank r the r-th share of its K blocks.
+template <class Cfg, bool kTail>
 __global__ void __launch_bounds__(Cfg::kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB, const GemmArgs args, int* status) {
@@ -223,8 +248,27 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   tc_fence_after();
 
   const uint32_t tmem_base = *tmem_holder;
+  // launched as a programmatic dependent: nothing below may read before the
+  // stream's earlier work is complete (the prologue above overlapped it)
+  if constexpr (kTail) griddep_wait();
   const Scheduler sched(args, BN, status);
   const int Kb = sched.Kb;
+  // This CTA's tiles, each over K blocks [kb0, kb1): blockIdx.x, + gridDim.x,
+  // ... below sched.total; or (kTail) tile t_begin if t_begin < t_end.  The
+  // whole-tile loops read the special registers directly: copies of them kept
+  // live through the roles cost registers the promotion warps do not have.
+  int t_begin = 0, t_end = 0, kb0 = 0, kb1 = Kb, part = 0;
+  if constexpr (kTail) {
+    const int tile_idx = blockIdx.x / args.split;  // clusters span consecutive CTAs
+    part = int(cluster_ctarank());
+    t_begin = tile_idx;
+    t_end = tile_idx < sched.total ? tile_idx + 1 : tile_idx;
+    kb0 = part * Kb / args.split;
+    kb1 = (part + 1) * Kb / args.split;
+  }
+  auto first_tile = [&](int tb) { return kTail ? tb : int(blockIdx.x); };
+  auto end_tile = [&](int te) { return kTail ? te : sched.total; };
+  auto tile_step = [&]() { return kTail ? 1 : int(gridDim.x); };
   auto fail = [&]() {
     *abort_flag = 1;
     raise_status(status, FP8GEMM_ERR_TIMEOUT);
@@ -238,10 +282,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < sched.total && ok; t += gridDim.x) {
+      for (int t = first_tile(t_begin); t < end_tile(t_end) && ok; t += tile_step()) {
         Tile tile;
         if (!sched.get(t, BN, tile)) continue;
-        for (int kb = 0; kb < Kb; ++kb, ++it) {
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1;
           if (!mbar_wait(&empty_bar[s], ph ^ 1, abort_flag)) {
@@ -268,10 +312,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       const uint32_t b_base = smem_addr(smB);
       uint32_t it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < sched.total && ok; t += gridDim.x) {
+      for (int t = first_tile(t_begin); t < end_tile(t_end) && ok; t += tile_step()) {
         Tile tile;
         if (!sched.get(t, BN, tile)) continue;
-        for (int kb = 0; kb < Kb; ++kb, ++it) {
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1;
           const int buf = it % NB;
@@ -308,7 +352,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     const int Nb = ceil_div(args.N, kBlockK);
     uint32_t it = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < sched.total && ok; t += gridDim.x) {
+    for (int t = first_tile(t_begin); t < end_tile(t_end) && ok; t += tile_step()) {
       Tile tile;
       if (!sched.get(t, BN, tile)) continue;
       const bool row_ok = row < tile.valid_rows;
@@ -323,11 +367,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 #pragma unroll
       for (int j = 0; j < Cfg::kColsPerWG / 2; ++j) acc[j] = make_float2(0.f, 0.f);
 
-      float sa_next = row_ok ? __ldg(sa_ptr) : 0.f;
-      float sb_next = cols_ok ? __ldg(sb_ptr) : 0.f;
-      for (int kb = 0; kb < Kb; ++kb, ++it) {
+      float sa_next = row_ok ? __ldg(sa_ptr + kb0) : 0.f;
+      float sb_next = cols_ok ? __ldg(sb_ptr + kb0) : 0.f;
+      for (int kb = kb0; kb < kb1; ++kb, ++it) {
         const float sc = sa_next * sb_next;
-        if (kb + 1 < Kb) {
+        if (kb + 1 < kb1) {
           sa_next = row_ok ? __ldg(sa_ptr + kb + 1) : 0.f;
           sb_next = cols_ok ? __ldg(sb_ptr + kb + 1) : 0.f;
         }
@@ -365,6 +409,16 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         }
       }
       if (!ok) break;
+      if constexpr (kTail) {
+        // stage this CTA's partial; the cluster sums and stores it below
+        float4* srow = reinterpret_cast<float4*>(smem) + (row * Stage<Cfg>::kPitch +
+                                                          wg * Cfg::kColsPerWG) / 4;
+#pragma unroll
+        for (int j4 = 0; j4 < Cfg::kColsPerWG / 4; ++j4)
+          srow[j4] = make_float4(acc[2 * j4].x, acc[2 * j4].y, acc[2 * j4 + 1].x,
+                                 acc[2 * j4 + 1].y);
+        continue;
+      }
       // epilogue: BF16 (round to nearest even), 16-byte stores; rows of D
       // are 16-byte aligned only when N % 8 == 0, else element stores
       if (row_ok && args.N % 8 != 0) {
@@ -398,6 +452,52 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     regs_decrease<Cfg::kLowRegs>();  // warps 10-11: no work
   }
 
+  if constexpr (kTail) {
+    // every CTA of the cluster has staged its partial (or, on an abort,
+    // whatever it holds: the status already says the result is void)
+    __syncwarp();
+    cluster_sync();
+    Tile tile;
+    if (warp < Cfg::kPromoWarps && t_begin < t_end && sched.get(t_begin, BN, tile)) {
+      // row band [r0, r1) of the tile: summed over the cluster's partials in
+      // rank order (deterministic), rounded to BF16, stored along rows
+      const int S = args.split;
+      const int r0 = part * kBlockM / S, r1 = (part + 1) * kBlockM / S;
+      constexpr int kF4 = BN / 4;  // float4s per row
+      const float4* mine = reinterpret_cast<const float4*>(smem);
+      for (int idx = r0 * kF4 + int(threadIdx.x); idx < r1 * kF4; idx += Cfg::kPromoWarps * 32) {
+        const int r = idx / kF4, c4 = idx % kF4;
+        const float4* p = mine + r * (Stage<Cfg>::kPitch / 4) + c4;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int q = 0; q < S; ++q) {
+          const float4 w = *map_shared_rank(p, uint32_t(q));
+          v.x += w.x;
+          v.y += w.y;
+          v.z += w.z;
+          v.w += w.w;
+        }
+        const int col = tile.n0 + 4 * c4;
+        if (r >= tile.valid_rows || col >= args.N) continue;
+        __nv_bfloat16* d = args.D + size_t(tile.row0 + r) * args.N + col;
+        const __nv_bfloat162 lo = __float22bfloat162_rn(make_float2(v.x, v.y));
+        const __nv_bfloat162 hi = __float22bfloat162_rn(make_float2(v.z, v.w));
+        if (args.N % 4 == 0) {  // col + 3 < N and the 8-byte store is aligned
+          uint2 u;
+          u.x = *reinterpret_cast<const uint32_t*>(&lo);
+          u.y = *reinterpret_cast<const uint32_t*>(&hi);
+          *reinterpret_cast<uint2*>(d) = u;
+        } else {
+          d[0] = lo.x;
+          if (col + 1 < args.N) d[1] = lo.y;
+          if (col + 2 < args.N) d[2] = hi.x;
+          if (col + 3 < args.N) d[3] = hi.y;
+        }
+      }
+    }
+    __syncwarp();
+    cluster_sync();  // no CTA leaves while another still reads its partial
+  }
+
   __syncthreads();
   if (warp == Cfg::kMmaWarp) {
     tc_fence_after();
@@ -405,40 +505,122 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   }
 }
 
+template <class Cfg, bool kTail>
+cudaError_t set_smem_attr() {
+  static bool done = false;  // per process; the attribute is per function
+  if (done) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<Cfg, kTail>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       int(Cfg::kSmemBytes));
+  if (e == cudaSuccess) done = true;
+  return e;
+}
+
+// Clusters of `s` split-instance CTAs that can be resident at once (0: none).
 template <class Cfg>
-cudaError_t run(const LaunchCtx& c, const GemmArgs& a) {
+int max_clusters(int dev, int s) {
+  static int known[64][kMaxSplit + 1] = {};  // 0 unknown, -1 none, else the count
+  int& k = known[dev & 63][s];
+  if (k == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(s);
+    cfg.blockDim = dim3(Cfg::kThreads);
+    cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = s;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<Cfg, true>, &cfg) != cudaSuccess) {
+      cudaGetLastError();  // a refused query leaves no sticky error
+      n = 0;
+    }
+    k = n > 0 ? n : -1;
+  }
+  return k > 0 ? k : 0;
+}
+
+// Parts per tile when all `tiles` fit in one wave: as many as leave every
+// tile's cluster resident at once, at most kMaxSplit, at least kMinPartKb K
+// blocks each, and only for K of kMinSplitKb blocks or more (below that the
+// cluster's fixed costs -- staging, two cluster barriers, the exchange --
+// ate the gain: neutral at 16 K blocks, 2.4 us slower at 4).  1: whole
+// tiles, the persistent instance.
+constexpr int kMinSplitKb = 32;
+constexpr int kMinPartKb = 4;
+
+template <class Cfg>
+int choose_split(const LaunchCtx& c, long long tiles, int Kb) {
+  if (tiles >= c.num_sms || Kb < kMinSplitKb) return 1;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  long long s = c.num_sms / tiles;
+  if (s > Kb / kMinPartKb) s = Kb / kMinPartKb;
+  if (s > kMaxSplit) s = kMaxSplit;
+  for (; s >= 2; --s)
+    if (max_clusters<Cfg>(dev, int(s)) >= tiles) return int(s);
+  return 1;
+}
+
+template <class Cfg>
+cudaError_t run(const LaunchCtx& c, GemmArgs a, int* launches) {
+  *launches = 0;
   CUtensorMap tmA, tmB;
   const uint64_t a_rows = a.mode == GemmMode::kMasked ? uint64_t(a.E) * a.M : uint64_t(a.M);
   const uint64_t b_rows = uint64_t(a.E) * a.N;
   if (!make_tmap_u8_sw128(&tmA, a.A, a_rows, a.K, kBlockM)) return cudaErrorInvalidValue;
   if (!make_tmap_u8_sw128(&tmB, a.B, b_rows, a.K, Cfg::BN)) return cudaErrorInvalidValue;
+  if (cudaError_t e = set_smem_attr<Cfg, false>()) return e;
+  if (cudaError_t e = set_smem_attr<Cfg, true>()) return e;
 
-  auto kern = gemm_tc_kernel<Cfg>;
-  static bool attr_set = false;  // per process; the attribute is per function
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(Cfg::kSmemBytes));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
   const int num_n = ceil_div(a.N, Cfg::BN);
-  long long tiles;
-  if (a.mode == GemmMode::kMasked)
-    tiles = (long long)a.E * ceil_div(a.M, kBlockM) * num_n;
-  else
-    tiles = (long long)ceil_div(a.M, kBlockM) * num_n;
-  const int grid = int(tiles < c.num_sms ? tiles : c.num_sms);
-  if (grid == 0) return cudaSuccess;
-  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, c.stream>>>(tmA, tmB, a, c.status);
-  return cudaGetLastError();
+  const bool masked = a.mode == GemmMode::kMasked;
+  // tiles: exact for the dense and contiguous forms; for the masked form an
+  // upper bound (the valid rows are on the device; clusters past the valid
+  // tiles find no work)
+  const long long tiles = (long long)(masked ? a.E : 1) * ceil_div(a.M, kBlockM) * num_n;
+  if (tiles == 0) return cudaSuccess;
+  a.split = choose_split<Cfg>(c, tiles, ceil_div(a.K, kBlockK));
+
+  if (a.split == 1) {
+    const int grid = int(tiles < c.num_sms ? tiles : c.num_sms);
+    gemm_tc_kernel<Cfg, false><<<grid, Cfg::kThreads, Cfg::kSmemBytes, c.stream>>>(tmA, tmB, a,
+                                                                                c.status);
+    if (cudaError_t e = cudaGetLastError()) return e;
+  } else {
+    // one cluster per tile, as a programmatic dependent (its prologue
+    // overlaps the end of the stream's earlier work)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(tiles * a.split));
+    cfg.blockDim = dim3(Cfg::kThreads);
+    cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+    cfg.stream = c.stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = unsigned(a.split);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    if (cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<Cfg, true>, tmA, tmB, a,
+                                           c.status))
+      return e;
+  }
+  *launches = 1;
+  return cudaSuccess;
 }
 
 }  // namespace
 
-cudaError_t launch_gemm_tc(const LaunchCtx& c, const GemmArgs& a) {
+cudaError_t launch_gemm_tc(const LaunchCtx& c, const GemmArgs& a, int* launches) {
   const bool wide = (a.N % 256 == 0) || a.N >= 2048;
-  if (wide) return run<TcCfg<256, 4>>(c, a);
-  return run<TcCfg<128, 6>>(c, a);
+  if (wide) return run<TcCfg<256, 4>>(c, a, launches);
+  return run<TcCfg<128, 6>>(c, a, launches);
 }
 
 }  // namespace fp8gemm
