@@ -32,7 +32,7 @@
 //
 // Split tiles: when every tile fits in one wave (fewer tiles than SMs, as for
 // a few hundred rows), most SMs would idle.  A second instance of the kernel
-// (kTail) then gives each tile a cluster of `split` CTAs, CTA r contracting
+// (kSplit) then gives each tile a cluster of `split` CTAs, CTA r contracting
 // the r-th share of the K blocks.  Each CTA stages its FP32 partial in its
 // own shared memory (the idle operand ring); after a cluster barrier CTA r
 // sums row band r of the tile over the cluster's CTAs, in rank order, through
@@ -194,10 +194,10 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
-// kTail = false: whole tiles, persistent over the CTAs.  kTail = true (all
+// kSplit = false: whole tiles, persistent over the CTAs.  kSplit = true (all
 // tiles fit in one wave): cluster c of args.split CTAs computes tile c, CTA
 // rank r the r-th share of its K blocks.
-template <class Cfg, bool kTail>
+template <class Cfg, bool kSplit>
 __global__ void __launch_bounds__(Cfg::kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB, const GemmArgs args, int* status) {
@@ -250,15 +250,15 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   const uint32_t tmem_base = *tmem_holder;
   // launched as a programmatic dependent: nothing below may read before the
   // stream's earlier work is complete (the prologue above overlapped it)
-  if constexpr (kTail) griddep_wait();
+  if constexpr (kSplit) griddep_wait();
   const Scheduler sched(args, BN, status);
   const int Kb = sched.Kb;
   // This CTA's tiles, each over K blocks [kb0, kb1): blockIdx.x, + gridDim.x,
-  // ... below sched.total; or (kTail) tile t_begin if t_begin < t_end.  The
+  // ... below sched.total; or (kSplit) tile t_begin if t_begin < t_end.  The
   // whole-tile loops read the special registers directly: copies of them kept
   // live through the roles cost registers the promotion warps do not have.
   int t_begin = 0, t_end = 0, kb0 = 0, kb1 = Kb, part = 0;
-  if constexpr (kTail) {
+  if constexpr (kSplit) {
     const int tile_idx = blockIdx.x / args.split;  // clusters span consecutive CTAs
     part = int(cluster_ctarank());
     t_begin = tile_idx;
@@ -266,9 +266,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     kb0 = part * Kb / args.split;
     kb1 = (part + 1) * Kb / args.split;
   }
-  auto first_tile = [&](int tb) { return kTail ? tb : int(blockIdx.x); };
-  auto end_tile = [&](int te) { return kTail ? te : sched.total; };
-  auto tile_step = [&]() { return kTail ? 1 : int(gridDim.x); };
+  auto first_tile = [&](int tb) { return kSplit ? tb : int(blockIdx.x); };
+  auto end_tile = [&](int te) { return kSplit ? te : sched.total; };
+  auto tile_step = [&]() { return kSplit ? 1 : int(gridDim.x); };
   auto fail = [&]() {
     *abort_flag = 1;
     raise_status(status, FP8GEMM_ERR_TIMEOUT);
@@ -409,7 +409,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         }
       }
       if (!ok) break;
-      if constexpr (kTail) {
+      if constexpr (kSplit) {
         // stage this CTA's partial; the cluster sums and stores it below
         float4* srow = reinterpret_cast<float4*>(smem) + (row * Stage<Cfg>::kPitch +
                                                           wg * Cfg::kColsPerWG) / 4;
@@ -452,7 +452,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     regs_decrease<Cfg::kLowRegs>();  // warps 10-11: no work
   }
 
-  if constexpr (kTail) {
+  if constexpr (kSplit) {
     // every CTA of the cluster has staged its partial (or, on an abort,
     // whatever it holds: the status already says the result is void)
     __syncwarp();
@@ -505,11 +505,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   }
 }
 
-template <class Cfg, bool kTail>
+template <class Cfg, bool kSplit>
 cudaError_t set_smem_attr() {
   static bool done = false;  // per process; the attribute is per function
   if (done) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<Cfg, kTail>,
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<Cfg, kSplit>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        int(Cfg::kSmemBytes));
   if (e == cudaSuccess) done = true;
