@@ -51,6 +51,13 @@
  *    Such a first call must therefore not happen during CUDA graph capture.
  *    Calls on different streams never share a workspace.  The reduction
  *    order is fixed, so results are deterministic.
+ *  - The dense and grouped paths for M > 64 split each output tile's K loop
+ *    over a thread-block cluster when all tiles fit in one wave of the SMs
+ *    and K spans at least 32 blocks of 128; the clusters' FP32 partials are
+ *    summed in a fixed order through distributed shared memory (no
+ *    workspace).  Results stay deterministic for a given shape; a split tile
+ *    may differ from the unsplit sum in the last bits of FP32 before the
+ *    BF16 rounding.
  */
 #ifndef FP8GEMM_H
 #define FP8GEMM_H
