@@ -152,7 +152,7 @@ def gemm_bytes(M, N, K, e_active=1, rows=None):
     """Algorithmic bytes of one block-scaled GEMM: A and its scales for the
     real rows, B and its scales for the active experts, D for the real rows."""
     rows = M if rows is None else rows
-    Kb = K // 128
+    Kb = -(-K // 128)  # a partial last K block carries a scale too
     Nb = -(-N // 128)
     return rows * K + 4 * rows * Kb + e_active * (N * K + 4 * Nb * Kb) + 2 * rows * N
 

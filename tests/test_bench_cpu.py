@@ -1,0 +1,89 @@
+"""Host-side logic of bench.py on the CPU: the reference arm's JSON line, the
+algorithmic byte count, the roofline bound, and the rule that ties a stored
+ncu traffic figure to the kernel source it was taken on."""
+
+import hashlib
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+
+def _run_bench(args, env_extra=None):
+    env = dict(os.environ)
+    env.update(env_extra or {})
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args],
+                          capture_output=True, text=True, timeout=600, env=env, cwd=ROOT)
+
+
+def test_reference_arm_prints_one_contract_line():
+    r = _run_bench(["--impl", "reference", "--steps", "3", "--warmup", "3"])
+    assert r.returncode == 0, r.stderr
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["steps"] == 3 and d["warmup"] == 3
+    assert d["value"] > 0 and d["unit"] == "TFLOP/s" and d["higher_is_better"] is True
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_other_ranks_are_silent():
+    r = _run_bench(["--impl", "reference", "--steps", "3", "--warmup", "3"],
+                   {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == ""
+
+
+def test_warmup_below_three_is_refused():
+    r = _run_bench(["--impl", "reference", "--steps", "3", "--warmup", "2"])
+    assert r.returncode != 0
+
+
+def test_gemm_bytes_counted_by_hand():
+    import bench
+    # dense 128 x 256 x 512: A 65536 + sA 128*4*4 + B 131072 + sB 2*4*4 + D 128*256*2
+    assert bench.gemm_bytes(128, 256, 512) == 65536 + 2048 + 131072 + 32 + 65536
+    # a partial last K block (K = 144) carries its own scale column
+    assert bench.gemm_bytes(1, 128, 144) == 144 + 2 * 4 + 128 * 144 + 2 * 4 + 256
+    # grouped: B and its scales once per active expert, A and D for the real rows
+    assert bench.gemm_bytes(0, 256, 256, e_active=3, rows=10) == (
+        10 * 256 + 10 * 2 * 4 + 3 * (256 * 256 + 2 * 2 * 4) + 10 * 256 * 2)
+
+
+def test_roof_takes_the_slower_bound():
+    import bench
+    peaks = {"hbm_gbs": 1000.0, "bf16": 500.0, "bf16_sustained": 400.0, "source": "test"}
+    # 1e12 FLOP at 800 TFLOP/s = 1.25 ms; 1e6 B at 1000 GB/s = 1 us: tensor-bound
+    r = bench._roof(1e12, 1e6, 2.5, peaks, sustained=True)
+    assert r["bound"] == "tensor" and r["roofline_frac"] == pytest.approx(0.5)
+    # 1e9 FLOP at the burst-derived 1000 TFLOP/s (1 us) against 1e9 B (1 ms): HBM-bound
+    r = bench._roof(1e9, 1e9, 4.0, peaks)
+    assert r["bound"] == "hbm" and r["roofline_frac"] == pytest.approx(0.25)
+    assert r["gbs"] == pytest.approx(250.0)
+
+
+def test_traffic_figure_only_for_the_source_it_was_taken_on(tmp_path, monkeypatch):
+    import bench
+    csrc = tmp_path / "fp8_fine_grained_e4m3_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (csrc / "k.cu").write_text("kernel v1\n")
+    digest = hashlib.sha256(b"kernel v1\n").hexdigest()[:16]
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(
+        {"case": {"sources": ["k.cu"], "source_hash": digest, "dram_bytes_per_launch": 1234}}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.traffic_from_profiles("case") == 1234
+    assert bench.traffic_from_profiles("other") is None
+    (csrc / "k.cu").write_text("kernel v2\n")
+    assert bench.traffic_from_profiles("case") is None
