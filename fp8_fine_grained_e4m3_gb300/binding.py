@@ -198,6 +198,21 @@ def _fmt(name):
     return FMT[name]
 
 
+def _u8_fmt(t, fmt, name):
+    """FP8 bytes in format `fmt`: a uint8 tensor, or a torch float8 tensor
+    whose own format agrees with `fmt` (viewed as uint8)."""
+    torch = _torch()
+    _fmt(fmt)
+    own = {torch.float8_e4m3fn: "e4m3", torch.float8_e5m2: "e5m2"}.get(t.dtype)
+    if own is not None:
+        if own != fmt:
+            raise TypeError(f"{name} is {t.dtype} but its format is given as {fmt!r}")
+        t = t.view(torch.uint8)
+    if t.dtype != torch.uint8:
+        raise TypeError(f"{name} must hold FP8 bytes (uint8 or a float8 dtype), got {t.dtype}")
+    return _dev(t, name)
+
+
 def fp8_quant_1x128_fmt(X, fmt, Q=None, sX=None, stream=None):
     """fp8_quant_1x128 with the output format ("e4m3" or "e5m2")."""
     torch = _torch()
@@ -208,8 +223,8 @@ def fp8_quant_1x128_fmt(X, fmt, Q=None, sX=None, stream=None):
         Q = torch.empty(X.shape, dtype=torch.uint8, device=X.device)
     if sX is None:
         sX = torch.empty((*X.shape[:-1], -(-K // 128)), dtype=torch.float32, device=X.device)
-    _check(lib().fp8_quant_1x128_fmt(_ptr(X), _ptr(_u8(Q, "Q")), _ptr(_f32(sX, "sX")), M, K,
-                                     _fmt(fmt), _stream(stream)), "fp8_quant_1x128_fmt")
+    _check(lib().fp8_quant_1x128_fmt(_ptr(X), _ptr(_u8_fmt(Q, fmt, "Q")), _ptr(_f32(sX, "sX")),
+                                     M, K, _fmt(fmt), _stream(stream)), "fp8_quant_1x128_fmt")
     return Q, sX
 
 
@@ -225,20 +240,16 @@ def fp8_quant_128x128_fmt(W, fmt, Q=None, sW=None, stream=None):
     if sW is None:
         shp = ((N + 127) // 128, -(-K // 128))
         sW = torch.empty(shp if squeeze else (E, *shp), dtype=torch.float32, device=W.device)
-    _check(lib().fp8_quant_128x128_fmt(_ptr(W3), _ptr(_u8(Q, "Q")), _ptr(_f32(sW, "sW")), E, N,
-                                       K, _fmt(fmt), _stream(stream)), "fp8_quant_128x128_fmt")
+    _check(lib().fp8_quant_128x128_fmt(_ptr(W3), _ptr(_u8_fmt(Q, fmt, "Q")), _ptr(_f32(sW, "sW")),
+                                       E, N, K, _fmt(fmt), _stream(stream)),
+           "fp8_quant_128x128_fmt")
     return Q, sW
 
 
 def fp8gemm_dense_fmt(A, sA, a_fmt, B, sB, b_fmt, D=None, stream=None):
     """fp8gemm_dense with operand formats ("e4m3" / "e5m2") for A and B."""
     torch = _torch()
-    A, B = _dev(A, "A"), _dev(B, "B")
-    if A.dtype in (torch.float8_e4m3fn, torch.float8_e5m2):
-        A = A.view(torch.uint8)
-    if B.dtype in (torch.float8_e4m3fn, torch.float8_e5m2):
-        B = B.view(torch.uint8)
-    A, B = _u8(A, "A"), _u8(B, "B")
+    A, B = _u8_fmt(A, a_fmt, "A"), _u8_fmt(B, b_fmt, "B")
     M, K = A.shape
     N = B.shape[0]
     if D is None:
@@ -337,7 +348,7 @@ def fp8gemm_grouped_masked(A, sA, B, sB, masked_m, D=None, stream=None):
 def fp8gemm_grouped_contiguous_fmt(A, sA, a_fmt, B, sB, b_fmt, m_indices, D=None, stream=None):
     """fp8gemm_grouped_contiguous with operand formats ("e4m3" / "e5m2")."""
     torch = _torch()
-    A, B = _u8(A, "A"), _u8(B, "B")
+    A, B = _u8_fmt(A, a_fmt, "A"), _u8_fmt(B, b_fmt, "B")
     M_pad, K = A.shape
     E, N = B.shape[0], B.shape[1]
     if D is None:
@@ -352,7 +363,7 @@ def fp8gemm_grouped_contiguous_fmt(A, sA, a_fmt, B, sB, b_fmt, m_indices, D=None
 def fp8gemm_grouped_masked_fmt(A, sA, a_fmt, B, sB, b_fmt, masked_m, D=None, stream=None):
     """fp8gemm_grouped_masked with operand formats ("e4m3" / "e5m2")."""
     torch = _torch()
-    A, B = _u8(A, "A"), _u8(B, "B")
+    A, B = _u8_fmt(A, a_fmt, "A"), _u8_fmt(B, b_fmt, "B")
     E, M_max, K = A.shape
     N = B.shape[1]
     if D is None:
