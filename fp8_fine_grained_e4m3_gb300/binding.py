@@ -118,19 +118,51 @@ def _u8(t, name):
         t = t.view(torch.uint8)
     if t.dtype != torch.uint8:
         raise TypeError(f"{name} must hold e4m3 bytes (uint8 or float8_e4m3fn), got {t.dtype}")
-    return _dev(t, name)
+    return t
 
 
 def _f32(t, name):
     if t.dtype != _torch().float32:
         raise TypeError(f"{name} must be float32, got {t.dtype}")
-    return _dev(t, name)
+    return t
 
 
 def _i32(t, name):
     if t.dtype != _torch().int32:
         raise TypeError(f"{name} must be int32, got {t.dtype}")
-    return _dev(t, name)
+    return t
+
+
+def _bf16(t, name):
+    if t.dtype != _torch().bfloat16:
+        raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+    return t
+
+
+def _cdiv(a, b):
+    return -(-a // b)
+
+
+def _need(t, name, elems, last=None):
+    """The library reads or writes exactly `elems` contiguous elements of t
+    (a row length of `last` when given): refuse a tensor of another size
+    before any pointer reaches a kernel, where it would be read or written
+    out of bounds."""
+    if t.numel() != elems or (last is not None and elems > 0 and t.shape[-1] != last):
+        want = f"{elems} elements" + (f" in rows of {last}" if last is not None else "")
+        raise ValueError(f"{name} has shape {tuple(t.shape)}; the call needs {want}")
+    return t
+
+
+def _shape_dense(A, sA, B, sB, D, M, N, K):
+    """Operand sizes of the dense forms: A [M, K], sA [M, ceil(K/128)],
+    B [N, K], sB [ceil(N/128), ceil(K/128)], D bf16 [M, N]."""
+    Kb = _cdiv(K, 128)
+    if B.dim() != 2 or B.shape[1] != K:
+        raise ValueError(f"B has shape {tuple(B.shape)}; the call needs [N, {K}]")
+    _need(sA, "sA", M * Kb, Kb)
+    _need(sB, "sB", _cdiv(N, 128) * Kb, Kb)
+    _need(_bf16(D, "D"), "D", M * N, N)
 
 
 def _dev(t, name):
@@ -141,8 +173,8 @@ def _dev(t, name):
     return t
 
 
-def _ptr(t):
-    return ctypes.c_void_p(t.data_ptr())
+def _ptr(t, name="tensor"):
+    return ctypes.c_void_p(_dev(t, name).data_ptr())
 
 
 # ------------------------------------------------------------ entry points
@@ -156,39 +188,57 @@ def fp8_quant_1x128(X, Q=None, sX=None, stream=None):
     if Q is None:
         Q = torch.empty(X.shape, dtype=torch.uint8, device=X.device)
     if sX is None:
-        sX = torch.empty((*X.shape[:-1], -(-K // 128)), dtype=torch.float32, device=X.device)
-    _check(lib().fp8_quant_1x128(_ptr(X), _ptr(_u8(Q, "Q")), _ptr(_f32(sX, "sX")), M, K,
+        sX = torch.empty((*X.shape[:-1], _cdiv(K, 128)), dtype=torch.float32, device=X.device)
+    _need(_u8(Q, "Q"), "Q", M * K, K)
+    _need(_f32(sX, "sX"), "sX", M * _cdiv(K, 128), _cdiv(K, 128))
+    _check(lib().fp8_quant_1x128(_ptr(X, "X"), _ptr(_u8(Q, "Q"), "Q"), _ptr(sX, "sX"), M, K,
                                  _stream(stream)), "fp8_quant_1x128")
     return Q, sX
+
+
+def _weights3(W):
+    W = _f32(W, "W")
+    if W.dim() not in (2, 3):
+        raise ValueError(f"W has shape {tuple(W.shape)}; the call needs [N, K] or [E, N, K]")
+    return W, W.dim() == 2, (W.unsqueeze(0) if W.dim() == 2 else W)
 
 
 def fp8_quant_128x128(W, Q=None, sW=None, stream=None):
     """W f32 [N, K] or [E, N, K] -> (Q u8 same shape, sW f32 [(E,) ceil(N/128), K/128])."""
     torch = _torch()
-    W = _f32(W, "W")
-    squeeze = W.dim() == 2
-    W3 = W.unsqueeze(0) if squeeze else W
+    W, squeeze, W3 = _weights3(W)
     E, N, K = W3.shape
+    shp = (_cdiv(N, 128), _cdiv(K, 128))
     if Q is None:
         Q = torch.empty(W.shape, dtype=torch.uint8, device=W.device)
     if sW is None:
-        shp = ((N + 127) // 128, -(-K // 128))
         sW = torch.empty(shp if squeeze else (E, *shp), dtype=torch.float32, device=W.device)
-    _check(lib().fp8_quant_128x128(_ptr(W3), _ptr(_u8(Q, "Q")), _ptr(_f32(sW, "sW")), E, N, K,
-                                   _stream(stream)), "fp8_quant_128x128")
+    _need(_u8(Q, "Q"), "Q", E * N * K, K)
+    _need(_f32(sW, "sW"), "sW", E * shp[0] * shp[1], shp[1])
+    _check(lib().fp8_quant_128x128(_ptr(W3, "W"), _ptr(_u8(Q, "Q"), "Q"), _ptr(sW, "sW"), E, N,
+                                   K, _stream(stream)), "fp8_quant_128x128")
     return Q, sW
+
+
+def _dense_mnk(A, B, name_a="A"):
+    if A.dim() != 2:
+        raise ValueError(f"{name_a} has shape {tuple(A.shape)}; the call needs [M, K]")
+    M, K = A.shape
+    if B.dim() != 2:
+        raise ValueError(f"B has shape {tuple(B.shape)}; the call needs [N, {K}]")
+    return M, B.shape[0], K
 
 
 def fp8gemm_dense(A, sA, B, sB, D=None, stream=None):
     """A u8 [M, K], sA [M, K/128], B u8 [N, K], sB [ceil(N/128), K/128] -> D bf16 [M, N]."""
     torch = _torch()
     A, B = _u8(A, "A"), _u8(B, "B")
-    M, K = A.shape
-    N = B.shape[0]
+    M, N, K = _dense_mnk(A, B)
     if D is None:
         D = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
-    _check(lib().fp8gemm_dense(_ptr(A), _ptr(_f32(sA, "sA")), _ptr(B), _ptr(_f32(sB, "sB")),
-                               _ptr(_dev(D, "D")), M, N, K, _stream(stream)), "fp8gemm_dense")
+    _shape_dense(A, _f32(sA, "sA"), B, _f32(sB, "sB"), D, M, N, K)
+    _check(lib().fp8gemm_dense(_ptr(A, "A"), _ptr(sA, "sA"), _ptr(B, "B"), _ptr(sB, "sB"),
+                               _ptr(D, "D"), M, N, K, _stream(stream)), "fp8gemm_dense")
     return D
 
 
@@ -210,7 +260,7 @@ def _u8_fmt(t, fmt, name):
         t = t.view(torch.uint8)
     if t.dtype != torch.uint8:
         raise TypeError(f"{name} must hold FP8 bytes (uint8 or a float8 dtype), got {t.dtype}")
-    return _dev(t, name)
+    return t
 
 
 def fp8_quant_1x128_fmt(X, fmt, Q=None, sX=None, stream=None):
@@ -222,27 +272,28 @@ def fp8_quant_1x128_fmt(X, fmt, Q=None, sX=None, stream=None):
     if Q is None:
         Q = torch.empty(X.shape, dtype=torch.uint8, device=X.device)
     if sX is None:
-        sX = torch.empty((*X.shape[:-1], -(-K // 128)), dtype=torch.float32, device=X.device)
-    _check(lib().fp8_quant_1x128_fmt(_ptr(X), _ptr(_u8_fmt(Q, fmt, "Q")), _ptr(_f32(sX, "sX")),
-                                     M, K, _fmt(fmt), _stream(stream)), "fp8_quant_1x128_fmt")
+        sX = torch.empty((*X.shape[:-1], _cdiv(K, 128)), dtype=torch.float32, device=X.device)
+    Q = _need(_u8_fmt(Q, fmt, "Q"), "Q", M * K, K)
+    _need(_f32(sX, "sX"), "sX", M * _cdiv(K, 128), _cdiv(K, 128))
+    _check(lib().fp8_quant_1x128_fmt(_ptr(X, "X"), _ptr(Q, "Q"), _ptr(sX, "sX"), M, K, _fmt(fmt),
+                                     _stream(stream)), "fp8_quant_1x128_fmt")
     return Q, sX
 
 
 def fp8_quant_128x128_fmt(W, fmt, Q=None, sW=None, stream=None):
     """fp8_quant_128x128 with the output format ("e4m3" or "e5m2")."""
     torch = _torch()
-    W = _f32(W, "W")
-    squeeze = W.dim() == 2
-    W3 = W.unsqueeze(0) if squeeze else W
+    W, squeeze, W3 = _weights3(W)
     E, N, K = W3.shape
+    shp = (_cdiv(N, 128), _cdiv(K, 128))
     if Q is None:
         Q = torch.empty(W.shape, dtype=torch.uint8, device=W.device)
     if sW is None:
-        shp = ((N + 127) // 128, -(-K // 128))
         sW = torch.empty(shp if squeeze else (E, *shp), dtype=torch.float32, device=W.device)
-    _check(lib().fp8_quant_128x128_fmt(_ptr(W3), _ptr(_u8_fmt(Q, fmt, "Q")), _ptr(_f32(sW, "sW")),
-                                       E, N, K, _fmt(fmt), _stream(stream)),
-           "fp8_quant_128x128_fmt")
+    Qb = _need(_u8_fmt(Q, fmt, "Q"), "Q", E * N * K, K)
+    _need(_f32(sW, "sW"), "sW", E * shp[0] * shp[1], shp[1])
+    _check(lib().fp8_quant_128x128_fmt(_ptr(W3, "W"), _ptr(Qb, "Q"), _ptr(sW, "sW"), E, N, K,
+                                       _fmt(fmt), _stream(stream)), "fp8_quant_128x128_fmt")
     return Q, sW
 
 
@@ -250,13 +301,13 @@ def fp8gemm_dense_fmt(A, sA, a_fmt, B, sB, b_fmt, D=None, stream=None):
     """fp8gemm_dense with operand formats ("e4m3" / "e5m2") for A and B."""
     torch = _torch()
     A, B = _u8_fmt(A, a_fmt, "A"), _u8_fmt(B, b_fmt, "B")
-    M, K = A.shape
-    N = B.shape[0]
+    M, N, K = _dense_mnk(A, B)
     if D is None:
         D = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
-    _check(lib().fp8gemm_dense_fmt(_ptr(A), _ptr(_f32(sA, "sA")), _fmt(a_fmt), _ptr(B),
-                                   _ptr(_f32(sB, "sB")), _fmt(b_fmt), _ptr(_dev(D, "D")), M, N,
-                                   K, _stream(stream)), "fp8gemm_dense_fmt")
+    _shape_dense(A, _f32(sA, "sA"), B, _f32(sB, "sB"), D, M, N, K)
+    _check(lib().fp8gemm_dense_fmt(_ptr(A, "A"), _ptr(sA, "sA"), _fmt(a_fmt), _ptr(B, "B"),
+                                   _ptr(sB, "sB"), _fmt(b_fmt), _ptr(D, "D"), M, N, K,
+                                   _stream(stream)), "fp8gemm_dense_fmt")
     return D
 
 
@@ -266,16 +317,23 @@ def fp8gemm_dense_quant_a(X, B, sB, D=None, Q=None, sA=None, stream=None):
     receive the quantised activations."""
     torch = _torch()
     X, B = _f32(X, "X"), _u8(B, "B")
-    M, K = X.shape
-    N = B.shape[0]
+    M, N, K = _dense_mnk(X, B, "X")
     if D is None:
         D = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
     if (Q is None) != (sA is None):
         raise ValueError("Q and sA go together: give both or neither")
-    qp = _ptr(_u8(Q, "Q")) if Q is not None else None
-    sp = _ptr(_f32(sA, "sA")) if sA is not None else None
-    _check(lib().fp8gemm_dense_quant_a(_ptr(X), qp, sp, _ptr(B), _ptr(_f32(sB, "sB")),
-                                       _ptr(_dev(D, "D")), M, N, K, _stream(stream)),
+    Kb = _cdiv(K, 128)
+    if B.shape[1] != K:
+        raise ValueError(f"B has shape {tuple(B.shape)}; the call needs [N, {K}]")
+    _need(_f32(sB, "sB"), "sB", _cdiv(N, 128) * Kb, Kb)
+    _need(_bf16(D, "D"), "D", M * N, N)
+    if Q is not None:
+        _need(_u8(Q, "Q"), "Q", M * K, K)
+        _need(_f32(sA, "sA"), "sA", M * Kb, Kb)
+    qp = _ptr(_u8(Q, "Q"), "Q") if Q is not None else None
+    sp = _ptr(sA, "sA") if sA is not None else None
+    _check(lib().fp8gemm_dense_quant_a(_ptr(X, "X"), qp, sp, _ptr(B, "B"), _ptr(sB, "sB"),
+                                       _ptr(D, "D"), M, N, K, _stream(stream)),
            "fp8gemm_dense_quant_a")
     return D
 
@@ -290,15 +348,18 @@ class Problem(ctypes.Structure):
 def problem_table(problems, out=None):
     """Device table for fp8gemm_grouped_table from (A, sA, B, sB, D) tensor
     tuples: a uint8 CUDA tensor of len(problems) * sizeof(Problem) bytes
-    (written into `out` when given, e.g. to update a table a graph captured)."""
+    (written into `out` when given, e.g. to update a table a graph captured).
+    Every entry's tensors are checked against its (M, N, K) here, since the
+    kernel only sees the pointers."""
     torch = _torch()
     arr = (Problem * len(problems))()
     for e, (A, sA, B, sB, D) in zip(arr, problems):
         A, B = _u8(A, "A"), _u8(B, "B")
-        e.A, e.sA, e.B = A.data_ptr(), _f32(sA, "sA").data_ptr(), B.data_ptr()
-        e.sB, e.D = _f32(sB, "sB").data_ptr(), _dev(D, "D").data_ptr()
-        e.M, e.K = A.shape
-        e.N = B.shape[0]
+        M, N, K = _dense_mnk(A, B)
+        _shape_dense(A, _f32(sA, "sA"), B, _f32(sB, "sB"), D, M, N, K)
+        e.A, e.sA, e.B = _dev(A, "A").data_ptr(), _dev(sA, "sA").data_ptr(), _dev(B, "B").data_ptr()
+        e.sB, e.D = _dev(sB, "sB").data_ptr(), _dev(D, "D").data_ptr()
+        e.M, e.N, e.K = M, N, K
         e.reserved = 0
     host = torch.frombuffer(bytearray(bytes(arr)), dtype=torch.uint8)
     if out is None:
@@ -310,69 +371,97 @@ def problem_table(problems, out=None):
 def fp8gemm_grouped_table(table, num_problems, max_M, stream=None):
     """Run every problem of a device table (see problem_table); max_M bounds
     every entry's M (<= 64) and picks the kernel's padded width."""
-    _check(lib().fp8gemm_grouped_table(_ptr(_dev(table, "table")), int(num_problems),
-                                       int(max_M), _stream(stream)), "fp8gemm_grouped_table")
+    if table.numel() < int(num_problems) * ctypes.sizeof(Problem):
+        raise ValueError(f"table holds {table.numel()} bytes; {num_problems} entries need "
+                         f"{int(num_problems) * ctypes.sizeof(Problem)}")
+    _check(lib().fp8gemm_grouped_table(_ptr(table, "table"), int(num_problems), int(max_M),
+                                       _stream(stream)), "fp8gemm_grouped_table")
 
 
-def fp8gemm_grouped_contiguous(A, sA, B, sB, m_indices, D=None, stream=None):
-    """A u8 [M_pad, K], B u8 [E, N, K], m_indices i32 [M_pad] -> D bf16 [M_pad, N]."""
+def _shape_grouped(A, sA, B, sB, info, D, rows, N, K, E, info_len, a_name="A"):
+    """Operand sizes of the grouped forms: A holds `rows` rows of K bytes,
+    sA [rows, ceil(K/128)], B [E, N, K], sB [E, ceil(N/128), ceil(K/128)],
+    the index array `info_len` int32 entries, D bf16 [rows, N]."""
+    Kb = _cdiv(K, 128)
+    _need(A, a_name, rows * K, K)
+    _need(sA, "sA", rows * Kb, Kb)
+    if B.dim() != 3 or B.shape[0] != E or B.shape[2] != K:
+        raise ValueError(f"B has shape {tuple(B.shape)}; the call needs [{E}, N, {K}]")
+    _need(sB, "sB", E * _cdiv(N, 128) * Kb, Kb)
+    _need(info, "the index array", info_len)
+    _need(_bf16(D, "D"), "D", rows * N, N)
+
+
+def _contiguous(A, sA, B, sB, m_indices, D, a_fmt, b_fmt, stream, fmt_call):
     torch = _torch()
-    A, B = _u8(A, "A"), _u8(B, "B")
+    if A.dim() != 2 or B.dim() != 3:
+        raise ValueError(f"A {tuple(A.shape)} / B {tuple(B.shape)}: the call needs A [M_pad, K]"
+                         " and B [E, N, K]")
     M_pad, K = A.shape
     E, N = B.shape[0], B.shape[1]
     if D is None:
         D = torch.empty((M_pad, N), dtype=torch.bfloat16, device=A.device)
-    _check(lib().fp8gemm_grouped_contiguous(
-        _ptr(A), _ptr(_f32(sA, "sA")), _ptr(B), _ptr(_f32(sB, "sB")),
-        _ptr(_i32(m_indices, "m_indices")), _ptr(_dev(D, "D")), M_pad, N, K, E,
-        _stream(stream)), "fp8gemm_grouped_contiguous")
+    _shape_grouped(A, _f32(sA, "sA"), B, _f32(sB, "sB"), _i32(m_indices, "m_indices"), D,
+                   M_pad, N, K, E, M_pad)
+    if fmt_call:
+        rc = lib().fp8gemm_grouped_contiguous_fmt(
+            _ptr(A, "A"), _ptr(sA, "sA"), _fmt(a_fmt), _ptr(B, "B"), _ptr(sB, "sB"),
+            _fmt(b_fmt), _ptr(m_indices, "m_indices"), _ptr(D, "D"), M_pad, N, K, E,
+            _stream(stream))
+    else:
+        rc = lib().fp8gemm_grouped_contiguous(
+            _ptr(A, "A"), _ptr(sA, "sA"), _ptr(B, "B"), _ptr(sB, "sB"),
+            _ptr(m_indices, "m_indices"), _ptr(D, "D"), M_pad, N, K, E, _stream(stream))
+    _check(rc, "fp8gemm_grouped_contiguous" + ("_fmt" if fmt_call else ""))
     return D
+
+
+def _masked(A, sA, B, sB, masked_m, D, a_fmt, b_fmt, stream, fmt_call):
+    torch = _torch()
+    if A.dim() != 3 or B.dim() != 3:
+        raise ValueError(f"A {tuple(A.shape)} / B {tuple(B.shape)}: the call needs A "
+                         "[E, M_max, K] and B [E, N, K]")
+    E, M_max, K = A.shape
+    N = B.shape[1]
+    if D is None:
+        D = torch.empty((E, M_max, N), dtype=torch.bfloat16, device=A.device)
+    _shape_grouped(A, _f32(sA, "sA"), B, _f32(sB, "sB"), _i32(masked_m, "masked_m"), D,
+                   E * M_max, N, K, E, E)
+    if fmt_call:
+        rc = lib().fp8gemm_grouped_masked_fmt(
+            _ptr(A, "A"), _ptr(sA, "sA"), _fmt(a_fmt), _ptr(B, "B"), _ptr(sB, "sB"),
+            _fmt(b_fmt), _ptr(masked_m, "masked_m"), _ptr(D, "D"), E, M_max, N, K,
+            _stream(stream))
+    else:
+        rc = lib().fp8gemm_grouped_masked(
+            _ptr(A, "A"), _ptr(sA, "sA"), _ptr(B, "B"), _ptr(sB, "sB"),
+            _ptr(masked_m, "masked_m"), _ptr(D, "D"), E, M_max, N, K, _stream(stream))
+    _check(rc, "fp8gemm_grouped_masked" + ("_fmt" if fmt_call else ""))
+    return D
+
+
+def fp8gemm_grouped_contiguous(A, sA, B, sB, m_indices, D=None, stream=None):
+    """A u8 [M_pad, K], B u8 [E, N, K], m_indices i32 [M_pad] -> D bf16 [M_pad, N]."""
+    return _contiguous(_u8(A, "A"), sA, _u8(B, "B"), sB, m_indices, D, "e4m3", "e4m3", stream,
+                       False)
 
 
 def fp8gemm_grouped_masked(A, sA, B, sB, masked_m, D=None, stream=None):
     """A u8 [E, M_max, K], B u8 [E, N, K], masked_m i32 [E] -> D bf16 [E, M_max, N]
     (rows >= masked_m[e] are not written)."""
-    torch = _torch()
-    A, B = _u8(A, "A"), _u8(B, "B")
-    E, M_max, K = A.shape
-    N = B.shape[1]
-    if D is None:
-        D = torch.empty((E, M_max, N), dtype=torch.bfloat16, device=A.device)
-    _check(lib().fp8gemm_grouped_masked(
-        _ptr(A), _ptr(_f32(sA, "sA")), _ptr(B), _ptr(_f32(sB, "sB")),
-        _ptr(_i32(masked_m, "masked_m")), _ptr(_dev(D, "D")), E, M_max, N, K,
-        _stream(stream)), "fp8gemm_grouped_masked")
-    return D
+    return _masked(_u8(A, "A"), sA, _u8(B, "B"), sB, masked_m, D, "e4m3", "e4m3", stream, False)
 
 
 def fp8gemm_grouped_contiguous_fmt(A, sA, a_fmt, B, sB, b_fmt, m_indices, D=None, stream=None):
     """fp8gemm_grouped_contiguous with operand formats ("e4m3" / "e5m2")."""
-    torch = _torch()
-    A, B = _u8_fmt(A, a_fmt, "A"), _u8_fmt(B, b_fmt, "B")
-    M_pad, K = A.shape
-    E, N = B.shape[0], B.shape[1]
-    if D is None:
-        D = torch.empty((M_pad, N), dtype=torch.bfloat16, device=A.device)
-    _check(lib().fp8gemm_grouped_contiguous_fmt(
-        _ptr(A), _ptr(_f32(sA, "sA")), _fmt(a_fmt), _ptr(B), _ptr(_f32(sB, "sB")), _fmt(b_fmt),
-        _ptr(_i32(m_indices, "m_indices")), _ptr(_dev(D, "D")), M_pad, N, K, E,
-        _stream(stream)), "fp8gemm_grouped_contiguous_fmt")
-    return D
+    return _contiguous(_u8_fmt(A, a_fmt, "A"), sA, _u8_fmt(B, b_fmt, "B"), sB, m_indices, D,
+                       a_fmt, b_fmt, stream, True)
 
 
 def fp8gemm_grouped_masked_fmt(A, sA, a_fmt, B, sB, b_fmt, masked_m, D=None, stream=None):
     """fp8gemm_grouped_masked with operand formats ("e4m3" / "e5m2")."""
-    torch = _torch()
-    A, B = _u8_fmt(A, a_fmt, "A"), _u8_fmt(B, b_fmt, "B")
-    E, M_max, K = A.shape
-    N = B.shape[1]
-    if D is None:
-        D = torch.empty((E, M_max, N), dtype=torch.bfloat16, device=A.device)
-    _check(lib().fp8gemm_grouped_masked_fmt(
-        _ptr(A), _ptr(_f32(sA, "sA")), _fmt(a_fmt), _ptr(B), _ptr(_f32(sB, "sB")), _fmt(b_fmt),
-        _ptr(_i32(masked_m, "masked_m")), _ptr(_dev(D, "D")), E, M_max, N, K,
-        _stream(stream)), "fp8gemm_grouped_masked_fmt")
-    return D
+    return _masked(_u8_fmt(A, a_fmt, "A"), sA, _u8_fmt(B, b_fmt, "B"), sB, masked_m, D,
+                   a_fmt, b_fmt, stream, True)
 
 
 def fp8gemm_dense_small_m_noalloc(A, sA, B, sB, D, stream=None):
@@ -381,10 +470,10 @@ def fp8gemm_dense_small_m_noalloc(A, sA, B, sB, D, stream=None):
     library (shared by every call on the device; calls must not overlap on the
     GPU)."""
     A, B = _u8(A, "A"), _u8(B, "B")
-    M, K = A.shape
-    N = B.shape[0]
+    M, N, K = _dense_mnk(A, B)
+    _shape_dense(A, _f32(sA, "sA"), B, _f32(sB, "sB"), D, M, N, K)
     _check(lib().fp8gemm_dense_small_m_noalloc(
-        _ptr(A), _ptr(_f32(sA, "sA")), _ptr(B), _ptr(_f32(sB, "sB")), _ptr(_dev(D, "D")),
+        _ptr(A, "A"), _ptr(sA, "sA"), _ptr(B, "B"), _ptr(sB, "sB"), _ptr(D, "D"),
         M, N, K, _stream(stream)), "fp8gemm_dense_small_m_noalloc")
     return D
 
