@@ -237,13 +237,16 @@ def run_gpu(args, rank, world):
     # shape (about 80 % of the step); the other shape is listed beside it
     gemm_flops = [2.0 * c["M"] * c["N"] * c["K"] for c in cases]
     achieved = gemm_flops[0] / (gemm_ms[0] * 1e-3) / 1e12
-    peak = fp8_peak(peaks, sustained=True)
+    # each step is short (sub-ms) and starts after an L2 flush at full clock:
+    # the burst figure is the denominator; the sustained one is listed beside
+    peak = fp8_peak(peaks, sustained=False)
     roofline = {"kernel": "gemm_tc_kernel<BN=256> (fp8gemm_dense, M > 64), M=4096 N=7168 K=16384",
                 "bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1),
                 "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                "peak_source": (f"{peaks['source']} bf16 sustained x 2 (FP8/BF16 nominal "
-                                "ratio); the kernel runs back to back for seconds"),
-                "frac_of_burst_peak": round(achieved / fp8_peak(peaks, False), 4),
+                "peak_source": (f"{peaks['source']} bf16 burst x 2 (FP8/BF16 nominal ratio): "
+                                "the kernel is timed in sub-ms steps after an L2 flush"),
+                "frac_of_sustained_peak": round(achieved / fp8_peak(peaks, True), 4),
+                "measured_fp8_tflops": measure_library_fp8(*PREFILL_SHAPES[0], flush),
                 "traffic": traffic_from_profiles("gemm_tc_dense_4096x7168x16384"),
                 "algorithmic_bytes": gemm_bytes(*PREFILL_SHAPES[0]),
                 "per_shape": [{"M": c["M"], "N": c["N"], "K": c["K"],
@@ -353,6 +356,40 @@ def time_graph(fns, reps=4):
     en.record()
     torch.cuda.synchronize()
     return st.elapsed_time(en) / (reps * len(fns))
+
+
+def measure_library_fp8(M, N, K, flush, n=10):
+    """Context for the FP8 peak: cuBLAS's per-tensor-scaled FP8 GEMM
+    (torch._scaled_mm, one scale per operand, so no per-block promotion) on
+    the same shape, timed like the GEMM here (L2 flushed, CUDA events).  It is
+    not part of the hot path; None where the call is unavailable."""
+    import torch
+    try:
+        a = torch.randn(M, K, device="cuda").to(torch.float8_e4m3fn)
+        b = torch.randn(N, K, device="cuda").to(torch.float8_e4m3fn)
+        one = torch.tensor(1.0, device="cuda")
+
+        def f():
+            return torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        for _ in range(3):
+            f()
+        torch.cuda.synchronize()
+        ts = []
+        stream = torch.cuda.current_stream()
+        for i in range(n):
+            flush(i)
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            f()
+            e.record(stream)
+            ts.append((s, e))
+        torch.cuda.synchronize()
+        ms = sum(s.elapsed_time(e) for s, e in ts) / n
+        del a, b
+        return {"tflops": round(2.0 * M * N * K / (ms * 1e-3) / 1e12, 1), "us": round(1e3 * ms, 1),
+                "what": "cuBLAS per-tensor FP8 (torch._scaled_mm), same shape, no block scales"}
+    except Exception as exc:  # pragma: no cover - depends on the torch build
+        return {"unavailable": f"{type(exc).__name__}: {exc}"[:200]}
 
 
 def _roof(flops, nbytes, ms, peaks, sustained=False):
