@@ -53,6 +53,9 @@ SIGNATURES = [
     ("fp8gemm_get_device_status", _I, [_P, ctypes.POINTER(ctypes.c_int)]),
     ("fp8gemm_strerror", ctypes.c_char_p, [_I]),
     ("fp8gemm_num_kernel_launches", ctypes.c_uint64, []),
+    ("fp8gemm_release_workspaces", _I, [_P]),
+    ("fp8gemm_workspace_bytes", ctypes.c_uint64, []),
+    ("fp8gemm_set_wait_limit_ns", _I, [ctypes.c_uint64]),
 ]
 
 
@@ -484,3 +487,20 @@ def fp8gemm_get_device_status(stream=None) -> int:
     _check(lib().fp8gemm_get_device_status(_stream(stream), ctypes.byref(out)),
            "fp8gemm_get_device_status")
     return out.value
+
+
+def fp8gemm_release_workspaces(stream=None):
+    """Free the library's workspaces of `stream` (current stream by default)
+    on the current device, after synchronising it."""
+    _check(lib().fp8gemm_release_workspaces(_stream(stream)), "fp8gemm_release_workspaces")
+
+
+def workspace_bytes() -> int:
+    """Bytes of library-owned workspaces currently held (all devices, streams)."""
+    return int(lib().fp8gemm_workspace_bytes())
+
+
+def set_wait_limit_ns(ns: int):
+    """Time limit of every pipeline wait in kernels launched from now on
+    (process-wide); 0 restores the default (2 s)."""
+    _check(lib().fp8gemm_set_wait_limit_ns(int(ns)), "fp8gemm_set_wait_limit_ns")

@@ -26,17 +26,26 @@ __global__ void exchange_status(int* status) { g_status_taken = atomicExch(statu
 namespace {
 
 std::atomic<unsigned long long> g_launches{0};
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s
+std::atomic<unsigned long long> g_wait_ns{kDefaultWaitNs};
 
 struct DeviceInfo {
   int num_sms = 0;
   int cc_major = 0, cc_minor = 0;
   int* status = nullptr;
+  unsigned long long ctx = 0;  // context the device address above belongs to
   bool ok = false;
+};
+
+struct Workspace {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+  unsigned long long ctx = 0;  // context it was allocated in
 };
 
 std::mutex g_mu;
 std::map<int, DeviceInfo> g_devices;
-std::map<std::tuple<int, cudaStream_t, int>, std::pair<void*, size_t>> g_workspaces;
+std::map<std::tuple<int, cudaStream_t, int>, Workspace> g_workspaces;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -56,13 +65,57 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Looks up (once per device) the SM count, compute capability and the
-// device address of the status word.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+template <class Fn>
+Fn driver_fn(const char* name) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return reinterpret_cast<Fn>(p);
+}
+
+}  // namespace
+
+// Unique id of the calling thread's current CUDA context (0 if unknown).
+// Device addresses cached per device stay valid only within one context: a
+// cudaDeviceReset ends the primary context, and the next one gets a new id.
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_cur = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+  static CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_cur || !get_id || get_cur(&ctx) != CUDA_SUCCESS || !ctx ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+namespace {
+
+// Looks up (once per device and context) the SM count, compute capability
+// and the device address of the status word.
 int device_info(DeviceInfo* out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FP8GEMM_ERR_LAUNCH;
+  unsigned long long ctx = current_context_id();
+  if (ctx == 0) {  // no context yet on this thread: the runtime creates it
+    if (cudaFree(nullptr) != cudaSuccess) return FP8GEMM_ERR_LAUNCH;
+    ctx = current_context_id();
+  }
   std::lock_guard<std::mutex> lk(g_mu);
   auto it = g_devices.find(dev);
+  if (it != g_devices.end() && it->second.ctx != ctx) {
+    // a new context on this device: addresses cached for the old one are
+    // stale, and so are the old context's workspaces (freed with it)
+    g_devices.erase(it);
+    for (auto w = g_workspaces.begin(); w != g_workspaces.end();)
+      w = std::get<0>(w->first) == dev ? g_workspaces.erase(w) : std::next(w);
+    it = g_devices.end();
+  }
   if (it == g_devices.end()) {
     DeviceInfo d;
     if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
@@ -72,6 +125,7 @@ int device_info(DeviceInfo* out) {
             cudaSuccess)
       return FP8GEMM_ERR_LAUNCH;
     d.ok = d.cc_major == 10 && d.cc_minor == 3;
+    d.ctx = ctx;
     if (d.ok && cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_device_status) !=
                     cudaSuccess)
       return FP8GEMM_ERR_LAUNCH;
@@ -102,16 +156,18 @@ enum { kWsSplitK = 0, kWsQuantA = 1 };
 int workspace_for(cudaStream_t s, size_t bytes, void** out, int slot = kWsSplitK) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FP8GEMM_ERR_LAUNCH;
+  DeviceInfo d;  // drops the workspaces of an ended context first
+  if (int r = device_info(&d)) return r;
   std::lock_guard<std::mutex> lk(g_mu);
   auto key = std::make_tuple(dev, s, slot);
   auto it = g_workspaces.find(key);
-  if (it != g_workspaces.end() && it->second.second >= bytes) {
-    *out = it->second.first;
+  if (it != g_workspaces.end() && it->second.bytes >= bytes) {
+    *out = it->second.ptr;
     return FP8GEMM_OK;
   }
   if (it != g_workspaces.end()) {  // grow: the old buffer may still be in use on s
     if (cudaStreamSynchronize(s) != cudaSuccess) return FP8GEMM_ERR_LAUNCH;
-    cudaFree(it->second.first);
+    cudaFree(it->second.ptr);
     g_workspaces.erase(it);
   }
   void* p = nullptr;
@@ -122,7 +178,7 @@ int workspace_for(cudaStream_t s, size_t bytes, void** out, int slot = kWsSplitK
     cudaFree(p);
     return FP8GEMM_ERR_LAUNCH;
   }
-  g_workspaces[key] = std::make_pair(p, bytes);
+  g_workspaces[key] = Workspace{p, bytes, d.ctx};
   *out = p;
   return FP8GEMM_OK;
 }
@@ -185,6 +241,7 @@ int ctx_for(cudaStream_t stream, LaunchCtx* c) {
 
 namespace fp8gemm {
 int make_launch_ctx(cudaStream_t stream, LaunchCtx* c) { return ctx_for(stream, c); }
+unsigned long long wait_limit_ns() { return g_wait_ns.load(); }
 void count_kernel_launches(int n) { g_launches += n; }
 }  // namespace fp8gemm
 
@@ -366,6 +423,23 @@ int fp8gemm_get_device_status(fp8gemm_stream_t stream, int* out) {
                                 stream) != cudaSuccess ||
       cudaStreamSynchronize(stream) != cudaSuccess)
     return FP8GEMM_ERR_LAUNCH;
+  if (v == FP8GEMM_ERR_TIMEOUT) {
+    // a launch that gave up may have left a split-K reduction half done, its
+    // arrival counters not back at zero: drop every workspace of this device
+    // (after the device is idle) so that the next calls start from zeroed ones
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
+      return FP8GEMM_ERR_LAUNCH;
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (auto w = g_workspaces.begin(); w != g_workspaces.end();) {
+      if (std::get<0>(w->first) != dev) {
+        ++w;
+        continue;
+      }
+      cudaFree(w->second.ptr);
+      w = g_workspaces.erase(w);
+    }
+  }
   *out = v;
   return FP8GEMM_OK;
 }
@@ -388,5 +462,40 @@ const char* fp8gemm_strerror(int code) {
 }
 
 uint64_t fp8gemm_num_kernel_launches(void) { return g_launches.load(); }
+
+int fp8gemm_release_workspaces(fp8gemm_stream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FP8GEMM_ERR_LAUNCH;
+  DeviceInfo d;  // forgets workspaces of an ended context (not freed twice)
+  if (int r = device_info(&d)) return r;
+  std::lock_guard<std::mutex> lk(g_mu);
+  bool synced = false;
+  int rc = FP8GEMM_OK;
+  for (auto w = g_workspaces.begin(); w != g_workspaces.end();) {
+    if (std::get<0>(w->first) != dev || std::get<1>(w->first) != stream) {
+      ++w;
+      continue;
+    }
+    if (!synced) {  // work already enqueued on the stream may still use it
+      if (cudaStreamSynchronize(stream) != cudaSuccess) return FP8GEMM_ERR_LAUNCH;
+      synced = true;
+    }
+    if (cudaFree(w->second.ptr) != cudaSuccess) rc = FP8GEMM_ERR_LAUNCH;
+    w = g_workspaces.erase(w);
+  }
+  return rc;
+}
+
+int fp8gemm_set_wait_limit_ns(uint64_t ns) {
+  g_wait_ns.store(ns == 0 ? kDefaultWaitNs : ns);
+  return FP8GEMM_OK;
+}
+
+uint64_t fp8gemm_workspace_bytes(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  uint64_t total = 0;
+  for (const auto& w : g_workspaces) total += w.second.bytes;
+  return total;
+}
 
 }  // extern "C"

@@ -56,6 +56,9 @@ struct GemmArgs {
   // Parts per tile along K (persistent tensor-core GEMM, split instance:
   // one cluster of `split` CTAs per tile).  1: whole tiles.
   int split = 1;
+  // Time limit of every pipeline wait in the kernel (the launcher fills in
+  // the process-wide setting, fp8gemm_set_wait_limit_ns).
+  unsigned long long wait_ns = 2000000000ull;
 };
 
 constexpr int kMaxSplit = 8;  // parts (cluster CTAs) per split tile, at most
@@ -79,6 +82,11 @@ cudaError_t launch_gemm_table(const LaunchCtx& c, const fp8gemm_problem* tab, in
 int make_launch_ctx(cudaStream_t stream, LaunchCtx* c);
 // Adds to the host-side count of kernels enqueued.  Defined in api.cu.
 void count_kernel_launches(int n);
+// Unique id of the calling thread's current CUDA context, 0 if none: device
+// addresses cached per device are valid within one context only.  api.cu.
+unsigned long long current_context_id();
+// The pipeline-wait time limit kernels launched now get, in ns.  api.cu.
+unsigned long long wait_limit_ns();
 
 // Encodes a 2-D K-major uint8 tensor map with 128-byte swizzling:
 // rows x cols bytes, box of box_rows x 128 bytes.  Defined in api.cu.

@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 2)
         const long long u = u_begin + i;
         const int s = i % kStages;
         const uint32_t ph = (i / kStages) & 1;
-        if (!mbar_wait(&empty_bar[s], ph ^ 1, abort_flag)) {
+        if (!mbar_wait(&empty_bar[s], ph ^ 1, abort_flag, args.wait_ns)) {
           fail();
           break;
         }
@@ -202,8 +202,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 2)
         const uint32_t ph = (i / kStages) & 1;
         const int buf = i % NB;
         const uint32_t tph = (i / NB) & 1;
-        if (!mbar_wait(&tempty_bar[buf], tph ^ 1, abort_flag) ||
-            !mbar_wait(&full_bar[s], ph, abort_flag)) {
+        if (!mbar_wait(&tempty_bar[buf], tph ^ 1, abort_flag, args.wait_ns) ||
+            !mbar_wait(&full_bar[s], ph, abort_flag, args.wait_ns)) {
           fail();
           break;
         }
@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 2)
     // bounded barrier over the 128 promotion threads
     auto group_sync = [&]() -> bool {
       mbar_arrive(group_bar);
-      const bool r = mbar_wait(group_bar, gphase, abort_flag);
+      const bool r = mbar_wait(group_bar, gphase, abort_flag, args.wait_ns);
       gphase ^= 1;
       return r;
     };
@@ -265,7 +265,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 2)
         }
         const int buf = it % NB;
         const uint32_t tph = (it / NB) & 1;
-        if (!mbar_wait(&tfull_bar[buf], tph, abort_flag)) {
+        if (!mbar_wait(&tfull_bar[buf], tph, abort_flag, args.wait_ns)) {
           fail();
           ok = false;
           break;
@@ -496,8 +496,10 @@ int cluster_split(const LaunchCtx& c, int n_tiles, int Kb) {
 }
 
 template <class Cfg>
-cudaError_t run(const LaunchCtx& c, const GemmArgs& a, void* ws, size_t ws_bytes,
+cudaError_t run(const LaunchCtx& c, const GemmArgs& args, void* ws, size_t ws_bytes,
                 bool allow_cluster) {
+  GemmArgs a = args;
+  a.wait_ns = wait_limit_ns();
   const int Kb = ceil_div(a.K, kBlockK);
   const int n_tiles = ceil_div(a.N, 128);
   const long long U = (long long)n_tiles * Kb;

@@ -117,7 +117,8 @@ struct Walk {
 
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kCtasPerSm)
-    gemm_table_kernel(const fp8gemm_problem* __restrict__ tab, int P, int max_M, int* status) {
+    gemm_table_kernel(const fp8gemm_problem* __restrict__ tab, int P, int max_M, int* status,
+                      unsigned long long wait_ns) {
   constexpr int MP = Cfg::MP;
   constexpr int kStages = Cfg::kStages;
   constexpr int NB = Cfg::kTmemBufs;
@@ -185,7 +186,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kCtasPerSm)
       const int tile = int(item - w.first);
       for (int kb = 0; kb < q.Kb; ++kb, ++i) {
         const int s = i % kStages;
-        if (!mbar_wait(&empty_bar[s], ((i / kStages) & 1) ^ 1, abort_flag)) {
+        if (!mbar_wait(&empty_bar[s], ((i / kStages) & 1) ^ 1, abort_flag, wait_ns)) {
           fail();
           ok = false;
           break;
@@ -223,8 +224,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kCtasPerSm)
         for (int kb = 0; kb < w.cur.Kb; ++kb, ++i) {
           const int s = i % kStages;
           const int buf = i % NB;
-          if (!mbar_wait(&tempty_bar[buf], ((i / NB) & 1) ^ 1, abort_flag) ||
-              !mbar_wait(&full_bar[s], (i / kStages) & 1, abort_flag)) {
+          if (!mbar_wait(&tempty_bar[buf], ((i / NB) & 1) ^ 1, abort_flag, wait_ns) ||
+              !mbar_wait(&full_bar[s], (i / kStages) & 1, abort_flag, wait_ns)) {
             fail();
             ok = false;
             break;
@@ -257,7 +258,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kCtasPerSm)
     bool ok = true;
     auto group_sync = [&]() -> bool {
       mbar_arrive(group_bar);
-      const bool r = mbar_wait(group_bar, gphase, abort_flag);
+      const bool r = mbar_wait(group_bar, gphase, abort_flag, wait_ns);
       gphase ^= 1;
       return r;
     };
@@ -286,7 +287,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kCtasPerSm)
           if (!group_sync()) { fail(); ok = false; break; }
         }
         const int buf = i % NB;
-        if (!mbar_wait(&tfull_bar[buf], (i / NB) & 1, abort_flag)) {
+        if (!mbar_wait(&tfull_bar[buf], (i / NB) & 1, abort_flag, wait_ns)) {
           fail();
           ok = false;
           break;
@@ -361,7 +362,8 @@ cudaError_t run(const LaunchCtx& c, const fp8gemm_problem* tab, int P, int max_M
   attr.val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_table_kernel<Cfg>, tab, P, max_M, c.status);
+  return cudaLaunchKernelEx(&cfg, gemm_table_kernel<Cfg>, tab, P, max_M, c.status,
+                            wait_limit_ns());
 }
 
 }  // namespace

@@ -288,7 +288,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1;
-          if (!mbar_wait(&empty_bar[s], ph ^ 1, abort_flag)) {
+          if (!mbar_wait(&empty_bar[s], ph ^ 1, abort_flag, args.wait_ns)) {
             fail();
             ok = false;
             break;
@@ -320,8 +320,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           const uint32_t ph = (it / kStages) & 1;
           const int buf = it % NB;
           const uint32_t tph = (it / NB) & 1;
-          if (!mbar_wait(&tempty_bar[buf], tph ^ 1, abort_flag) ||
-              !mbar_wait(&full_bar[s], ph, abort_flag)) {
+          if (!mbar_wait(&tempty_bar[buf], tph ^ 1, abort_flag, args.wait_ns) ||
+              !mbar_wait(&full_bar[s], ph, abort_flag, args.wait_ns)) {
             fail();
             ok = false;
             break;
@@ -377,7 +377,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         }
         const int buf = it % NB;
         const uint32_t tph = (it / NB) & 1;
-        if (!mbar_wait(&tfull_bar[buf], tph, abort_flag)) {
+        if (!mbar_wait(&tfull_bar[buf], tph, abort_flag, args.wait_ns)) {
           fail();
           ok = false;
           break;
@@ -568,6 +568,7 @@ int choose_split(const LaunchCtx& c, long long tiles, int Kb) {
 template <class Cfg>
 cudaError_t run(const LaunchCtx& c, GemmArgs a, int* launches) {
   *launches = 0;
+  a.wait_ns = wait_limit_ns();
   CUtensorMap tmA, tmB;
   const uint64_t a_rows = a.mode == GemmMode::kMasked ? uint64_t(a.E) * a.M : uint64_t(a.M);
   const uint64_t b_rows = uint64_t(a.E) * a.N;

@@ -9,8 +9,9 @@
 // or fragments the pool; a latency-critical loop that cannot afford
 // cudaMalloc's implicit device-wide synchronisation.  This entry point calls
 // no allocating routine at all.  The price is a fixed footprint: the array
-// below (kScratchBytes, about 10.3 MiB) exists on every GPU that loads the
-// library, for the life of the process, whether or not it is used.
+// below (kScratchBytes, 10.25 MiB) is created on a GPU when this file's module
+// is loaded there -- under CUDA's default lazy loading, by the first call of
+// this entry point on that GPU -- and stays until the process exits.
 //
 // Sharing: every call on a device uses the same array.  Calls that overlap on
 // the GPU (for example on two streams at once) race on it and give wrong
@@ -40,22 +41,28 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
 void* g_scratch_addr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device, looked up once
-// per device: the first call on each device does this set-up, so that first
-// call belongs before any CUDA stream capture.
+// per device and context with that device current: the first call on each
+// device does this set-up (and loads the module that holds the array), so
+// that first call belongs before any CUDA stream capture.  After a
+// cudaDeviceReset the device has a new context and the address is looked up
+// again.
 int scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FP8GEMM_ERR_LAUNCH;
   if (dev < 0 || dev >= kMaxDevices) return FP8GEMM_ERR_LAUNCH;
+  const unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
+  if (!g_scratch_addr[dev] || g_scratch_ctx[dev] != ctx || ctx == 0) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
       cudaGetLastError();
       return FP8GEMM_ERR_LAUNCH;
     }
     g_scratch_addr[dev] = p;
+    g_scratch_ctx[dev] = current_context_id();
   }
   *out = g_scratch_addr[dev];
   return FP8GEMM_OK;

@@ -46,11 +46,13 @@
  *  - The dense path for M <= 64 may split K across CTAs and reduce partial
  *    sums through a per-(device, stream) workspace that the library allocates
  *    with cudaMalloc on the first such call on that stream (about 10 MB, kept
- *    until process exit) and zeroes on that stream; fp8gemm_dense_quant_a at
+ *    until released or process exit) and zeroes on that stream; fp8gemm_dense_quant_a at
  *    M > 64 without Q/sA keeps its quantised A in a second per-stream buffer.
  *    Such a first call must therefore not happen during CUDA graph capture.
  *    Calls on different streams never share a workspace.  The reduction
- *    order is fixed, so results are deterministic.
+ *    order is fixed, so results are deterministic.  A caller that retires a
+ *    stream frees its workspaces with fp8gemm_release_workspaces() before
+ *    destroying it; fp8gemm_workspace_bytes() reports what is held.
  *  - The dense and grouped paths for M > 64 split each output tile's K loop
  *    over a thread-block cluster when all tiles fit in one wave of the SMs
  *    and K spans at least 32 blocks of 128; the clusters' FP32 partials are
@@ -277,12 +279,16 @@ int fp8gemm_grouped_table(const fp8gemm_problem* problems, int num_problems, int
  * implicit synchronisation.  (The pages this library follows have no
  * counterpart; this variant exists for that constraint only.)
  *
- * It allocates nothing: its split-K scratch is a fixed array of about
- * 10.3 MiB in the library's device image, present on every GPU that loads the
- * library until the process exits.  The first call on each device does a
- * one-time set-up -- it looks up that array's device address with
- * cudaGetSymbolAddress -- and later calls reuse it; make that first call on
- * each device before any CUDA stream capture begins.
+ * It allocates nothing: its split-K scratch is a fixed array of 10.25 MiB in
+ * the library's device image.  The array is created on a GPU when the part of
+ * the library that holds it is loaded there -- under CUDA's default lazy
+ * module loading, by the first call of this entry point on that GPU -- and
+ * stays until the process exits.  That first call on each device also does a
+ * one-time set-up (it looks up the array's device address with
+ * cudaGetSymbolAddress); later calls reuse the address.  So make the first
+ * call on each device during start-up, before the memory budget is fixed and
+ * before any CUDA stream capture begins.  After a cudaDeviceReset the next
+ * call repeats the set-up in the new context.
  *
  * Arguments, layouts, ownership and results are those of fp8gemm_dense, with
  * these limits: M <= 64 and N <= 8388608 (ceil(N/128) arrival counters must
@@ -305,7 +311,10 @@ int fp8gemm_dense_small_m_noalloc(const uint8_t* A, const float* sA, const uint8
  * (a one-thread kernel on `stream`), then synchronise `stream`:
  * *out = FP8GEMM_OK, FP8GEMM_ERR_DEVICE_STATUS or FP8GEMM_ERR_TIMEOUT.  A
  * condition raised meanwhile by a kernel on another stream is either
- * returned here or left for the next read.  Returns FP8GEMM_OK, or
+ * returned here or left for the next read.  On FP8GEMM_ERR_TIMEOUT the call
+ * also synchronises the device and frees every library workspace of it (a
+ * launch that gave up can leave a split-K reduction's counters mid-count);
+ * the next calls allocate fresh, zeroed ones.  Returns FP8GEMM_OK, or
  * FP8GEMM_ERR_NULL / FP8GEMM_ERR_LAUNCH if `out` is NULL or the CUDA calls
  * fail.
  */
@@ -317,6 +326,40 @@ const char* fp8gemm_strerror(int code);
 /* fp8gemm_num_kernel_launches -- kernels this process enqueued through the
  * library so far (all devices); a host-side counter for launch accounting. */
 uint64_t fp8gemm_num_kernel_launches(void);
+
+/*
+ * fp8gemm_release_workspaces -- free every library-owned workspace of
+ * `stream` on the current device (the split-K buffer of the decode path and
+ * the quantised-activation buffer of fp8gemm_dense_quant_a).  It first
+ * synchronises `stream`, since work enqueued there may still use them; the
+ * next call that needs a workspace on that stream allocates it again.  Call
+ * it before cudaStreamDestroy for streams that are retired: a stream handle
+ * that is destroyed and later reused by the runtime would otherwise find its
+ * predecessor's buffer.  Not allowed during stream capture.  Returns
+ * FP8GEMM_OK, or FP8GEMM_ERR_LAUNCH if a CUDA call fails.
+ * (The pages have no counterpart: this is resource management of the
+ * library's own buffers.)
+ */
+int fp8gemm_release_workspaces(fp8gemm_stream_t stream);
+
+/* fp8gemm_workspace_bytes -- bytes of library-owned workspaces currently held
+ * (all devices and streams). */
+uint64_t fp8gemm_workspace_bytes(void);
+
+/*
+ * fp8gemm_set_wait_limit_ns -- time limit, in nanoseconds of the GPU's global
+ * timer, of every pipeline wait inside the GEMM kernels launched after this
+ * call (process-wide; 0 restores the default of 2 s).  A wait that exceeds
+ * it is treated as a deadlock: the CTA stops, lets its copies and tensor-core
+ * operations in flight finish, frees its TMEM, exits, and the status word
+ * reads FP8GEMM_ERR_TIMEOUT (results of that launch are void).  A short limit
+ * makes the failure path observable in tests; production code keeps the
+ * default.  The hardware cluster barriers of the split-K forms have no limit
+ * of their own; every thread reaches them because every wait before them is
+ * bounded.  Returns FP8GEMM_OK.  (The pages have no counterpart: this is the
+ * library's deadlock detection.)
+ */
+int fp8gemm_set_wait_limit_ns(uint64_t ns);
 
 #ifdef __cplusplus
 }

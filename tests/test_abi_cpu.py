@@ -94,6 +94,7 @@ def test_host_validation_needs_no_gpu(lib):
     assert lib.fp8gemm_grouped_table(None, 0, 16, s) == b.OK
     assert lib.fp8gemm_get_device_status(s, None) == b.ERR_NULL
     assert isinstance(lib.fp8gemm_num_kernel_launches(), int)
+    assert lib.fp8gemm_workspace_bytes() == 0  # nothing allocated without a GPU
 
 
 def test_problem_struct_layout():
