@@ -456,7 +456,17 @@ def measure_configs(peaks, dev):
             r = _roof(2 * M * N * K, nb, ms_q, peaks)
             r["timing"] = "CUDA graph, 24 rotating weight copies; quantiser + GEMM, 2 launches"
             res[f"decode_quant_a_{M}x{N}x{K}"] = r
-            del copies, fns, fns_q, X
+            # Constant weights declared read-only (FP8GEMM_FLAG_B_READ_ONLY):
+            # each GEMM stages its first weight tiles while the one before
+            # it finishes
+            fns_ro = [(lambda Bc=Bc, sBc=sBc: b.fp8gemm_dense_ex(A8, sA, "e4m3", Bc, sBc, "e4m3",
+                                                                 D=D, flags=b.FLAG_B_READ_ONLY))
+                      for Bc, sBc in copies]
+            ms_ro = time_graph(fns_ro, reps=4)
+            r = _roof(2 * M * N * K, gemm_bytes(M, N, K), ms_ro, peaks)
+            r["timing"] = "CUDA graph, 24 rotating weight copies; weights declared read-only"
+            res[f"decode_ro_{M}x{N}x{K}"] = r
+            del copies, fns, fns_q, fns_ro, X
 
     # mixed formats: e5m2 A (a gradient) against e4m3 B, large and decode shapes
     for (M, N, K) in ((4096, 7168, 16384), (16, 7168, 2048)):

@@ -27,7 +27,9 @@ ERR_DEVICE_STATUS = -6
 ERR_TIMEOUT = -7
 ERR_SCRATCH_LIMIT = -8
 ERR_FORMAT = -9
+ERR_FLAGS = -10
 FMT = {"e4m3": 0, "e5m2": 1}  # FP8GEMM_FMT_*
+FLAG_B_READ_ONLY = 1  # FP8GEMM_FLAG_B_READ_ONLY
 
 _lib = None
 _lock = threading.Lock()
@@ -42,6 +44,7 @@ SIGNATURES = [
     ("fp8_quant_1x128_fmt", _I, [_P, _P, _P, _I, _I, _I, _P]),
     ("fp8_quant_128x128_fmt", _I, [_P, _P, _P, _I, _I, _I, _I, _P]),
     ("fp8gemm_dense_fmt", _I, [_P, _P, _I, _P, _P, _I, _P, _I, _I, _I, _P]),
+    ("fp8gemm_dense_ex", _I, [_P, _P, _I, _P, _P, _I, _P, _I, _I, _I, ctypes.c_uint, _P]),
     ("fp8gemm_grouped_table", _I, [_P, _I, _I, _P]),
     ("fp8gemm_grouped_contiguous_fmt", _I,
      [_P, _P, _I, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P]),
@@ -311,6 +314,22 @@ def fp8gemm_dense_fmt(A, sA, a_fmt, B, sB, b_fmt, D=None, stream=None):
     _check(lib().fp8gemm_dense_fmt(_ptr(A, "A"), _ptr(sA, "sA"), _fmt(a_fmt), _ptr(B, "B"),
                                    _ptr(sB, "sB"), _fmt(b_fmt), _ptr(D, "D"), M, N, K,
                                    _stream(stream)), "fp8gemm_dense_fmt")
+    return D
+
+
+def fp8gemm_dense_ex(A, sA, a_fmt, B, sB, b_fmt, D=None, flags=0, stream=None):
+    """fp8gemm_dense_fmt with flags, e.g. FLAG_B_READ_ONLY: B and sB are not
+    written by any kernel still running when this one starts (constant
+    weights), so the decode path may stage them before its dependency wait."""
+    torch = _torch()
+    A, B = _u8_fmt(A, a_fmt, "A"), _u8_fmt(B, b_fmt, "B")
+    M, N, K = _dense_mnk(A, B)
+    if D is None:
+        D = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    _shape_dense(A, _f32(sA, "sA"), B, _f32(sB, "sB"), D, M, N, K)
+    _check(lib().fp8gemm_dense_ex(_ptr(A, "A"), _ptr(sA, "sA"), _fmt(a_fmt), _ptr(B, "B"),
+                                  _ptr(sB, "sB"), _fmt(b_fmt), _ptr(D, "D"), M, N, K,
+                                  int(flags), _stream(stream)), "fp8gemm_dense_ex")
     return D
 
 

@@ -282,13 +282,14 @@ int fp8_quant_128x128(const float* W, uint8_t* Q, float* sW, int E, int N, int K
   return fp8_quant_128x128_fmt(W, Q, sW, E, N, K, FP8GEMM_FMT_E4M3, stream);
 }
 
-int fp8gemm_dense_fmt(const uint8_t* A, const float* sA, int a_fmt, const uint8_t* B,
-                      const float* sB, int b_fmt, void* D, int M, int N, int K,
-                      fp8gemm_stream_t stream) {
+int fp8gemm_dense_ex(const uint8_t* A, const float* sA, int a_fmt, const uint8_t* B,
+                     const float* sB, int b_fmt, void* D, int M, int N, int K, unsigned flags,
+                     fp8gemm_stream_t stream) {
   if (int r = check_common(M, N, K)) return r;
   if ((a_fmt != FP8GEMM_FMT_E4M3 && a_fmt != FP8GEMM_FMT_E5M2) ||
       (b_fmt != FP8GEMM_FMT_E4M3 && b_fmt != FP8GEMM_FMT_E5M2))
     return FP8GEMM_ERR_FORMAT;
+  if (flags & ~unsigned(FP8GEMM_FLAG_B_READ_ONLY)) return FP8GEMM_ERR_FLAGS;
   if (M == 0 || N == 0) return FP8GEMM_OK;
   if (!A || !sA || !B || !sB || !D) return FP8GEMM_ERR_NULL;
   if (!aligned16(A) || !aligned16(sA) || !aligned16(B) || !aligned16(sB) || !aligned16(D))
@@ -299,6 +300,7 @@ int fp8gemm_dense_fmt(const uint8_t* A, const float* sA, int a_fmt, const uint8_
              M, N, K, 1};
   a.a_fmt = a_fmt;
   a.b_fmt = b_fmt;
+  a.b_read_only = (flags & FP8GEMM_FLAG_B_READ_ONLY) ? 1 : 0;
   if (M <= kSmallM) {
     if (!small_m_uses_workspace(c, a)) return finish(launch_gemm_small_m_any(c, a, nullptr, 0), 1);
     const size_t bytes = small_m_workspace_bytes(c.num_sms, N);
@@ -307,6 +309,12 @@ int fp8gemm_dense_fmt(const uint8_t* A, const float* sA, int a_fmt, const uint8_
     return finish(launch_gemm_small_m_any(c, a, ws, bytes), 1);
   }
   return run_gemm_tc(c, a);
+}
+
+int fp8gemm_dense_fmt(const uint8_t* A, const float* sA, int a_fmt, const uint8_t* B,
+                      const float* sB, int b_fmt, void* D, int M, int N, int K,
+                      fp8gemm_stream_t stream) {
+  return fp8gemm_dense_ex(A, sA, a_fmt, B, sB, b_fmt, D, M, N, K, 0u, stream);
 }
 
 int fp8gemm_dense(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB, void* D,
@@ -457,6 +465,7 @@ const char* fp8gemm_strerror(int code) {
     case FP8GEMM_ERR_SCRATCH_LIMIT:
       return "problem exceeds the fixed scratch of fp8gemm_dense_small_m_noalloc (M <= 64)";
     case FP8GEMM_ERR_FORMAT: return "unknown FP8 format (FP8GEMM_FMT_E4M3 or FP8GEMM_FMT_E5M2)";
+    case FP8GEMM_ERR_FLAGS: return "unknown flag bits (FP8GEMM_FLAG_*)";
     default: return "unknown status";
   }
 }

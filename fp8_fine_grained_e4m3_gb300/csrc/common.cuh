@@ -59,6 +59,10 @@ struct GemmArgs {
   // Time limit of every pipeline wait in the kernel (the launcher fills in
   // the process-wide setting, fp8gemm_set_wait_limit_ns).
   unsigned long long wait_ns = 2000000000ull;
+  // The caller's promise (FP8GEMM_FLAG_B_READ_ONLY) that no kernel still
+  // running when this one starts writes B or sB: a programmatic dependent may
+  // then load weights before waiting for the kernels ahead of it.
+  int b_read_only = 0;
 };
 
 constexpr int kMaxSplit = 8;  // parts (cluster CTAs) per split tile, at most

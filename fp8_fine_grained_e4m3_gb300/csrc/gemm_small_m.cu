@@ -165,12 +165,26 @@ __global__ void __launch_bounds__(Cfg::kThreads, 2)
       // Pull this CTA's weight tiles towards L2 while the previous kernel in
       // the stream may still be running (a prefetch cannot return stale data);
       // every load into shared memory waits for that kernel.
+      // With the caller's promise that no kernel still running writes the
+      // weights (args.b_read_only), the first kStages weight tiles go
+      // straight into shared memory instead: their full barriers are armed
+      // for weights and activations, the activation halves follow the wait.
+      const int pre = args.b_read_only ? (n_units < kStages ? n_units : kStages) : 0;
       for (int i = 0; i < n_units; ++i) {
         const long long u = u_begin + i;
-        tma_prefetch_l2_2d(&tmW, int(u % Kb) * kBlockK, int(u / Kb) * 128);
+        if (i < pre) {  // first use of each stage: nothing to wait for
+          mbar_arrive_expect_tx(&full_bar[i], Cfg::kWBytes + Cfg::kXBytes);
+          tma_load_2d_hint(smW + i * Cfg::kWBytes, &tmW, &full_bar[i], int(u % Kb) * kBlockK,
+                           int(u / Kb) * 128, pol_stream);
+        } else {
+          tma_prefetch_l2_2d(&tmW, int(u % Kb) * kBlockK, int(u / Kb) * 128);
+        }
       }
       griddep_wait();
-      int i = 0;
+      for (int i = 0; i < pre; ++i)
+        tma_load_2d_hint(smX + i * Cfg::kXBytes, &tmX, &full_bar[i],
+                         int((u_begin + i) % Kb) * kBlockK, 0, pol_keep);
+      int i = pre;
       for (; i < n_units; ++i) {
         const long long u = u_begin + i;
         const int s = i % kStages;

@@ -82,7 +82,8 @@ enum fp8gemm_status {
   FP8GEMM_ERR_DEVICE_STATUS = -6,
   FP8GEMM_ERR_TIMEOUT = -7,
   FP8GEMM_ERR_SCRATCH_LIMIT = -8,
-  FP8GEMM_ERR_FORMAT = -9
+  FP8GEMM_ERR_FORMAT = -9,
+  FP8GEMM_ERR_FLAGS = -10
 };
 
 /* FP8 operand formats of the *_fmt calls ("news.rkmt.cn/news/5092" section
@@ -158,6 +159,31 @@ int fp8gemm_dense(const uint8_t* A, const float* sA, const uint8_t* B, const flo
 int fp8gemm_dense_fmt(const uint8_t* A, const float* sA, int a_fmt, const uint8_t* B,
                       const float* sB, int b_fmt, void* D, int M, int N, int K,
                       fp8gemm_stream_t stream);
+
+/* Flags of fp8gemm_dense_ex. */
+enum fp8gemm_flags {
+  /* The caller promises that B and sB are not written by any kernel that
+   * may still be running when this call's kernel starts (e.g. constant
+   * weights).  The decode path (M <= 64), launched as a programmatic
+   * dependent of the kernel before it, may then stage its first weight tiles
+   * into shared memory while that kernel finishes, instead of waiting for it
+   * first; activations, scales of A and D still wait.  Breaking the promise
+   * gives results computed from stale weights.  Other paths accept the flag
+   * and ignore it. */
+  FP8GEMM_FLAG_B_READ_ONLY = 1u
+};
+
+/*
+ * fp8gemm_dense_ex -- fp8gemm_dense_fmt with flags (FP8GEMM_FLAG_*; 0 gives
+ * exactly fp8gemm_dense_fmt).  Unknown flag bits return FP8GEMM_ERR_FLAGS.
+ * Arithmetic, layouts and limits are those of fp8gemm_dense.  (The pages
+ * describe weights that stay fixed across calls -- quantised once, offline,
+ * "lpnh.cn/news/2822121" section 2.3 -- which is what the flag lets the
+ * kernel exploit.)
+ */
+int fp8gemm_dense_ex(const uint8_t* A, const float* sA, int a_fmt, const uint8_t* B,
+                     const float* sB, int b_fmt, void* D, int M, int N, int K, unsigned flags,
+                     fp8gemm_stream_t stream);
 
 /*
  * fp8gemm_dense_quant_a -- fp8gemm_dense on FP32 activations: A and sA are

@@ -95,6 +95,10 @@ def test_host_validation_needs_no_gpu(lib):
     assert lib.fp8gemm_get_device_status(s, None) == b.ERR_NULL
     assert isinstance(lib.fp8gemm_num_kernel_launches(), int)
     assert lib.fp8gemm_workspace_bytes() == 0  # nothing allocated without a GPU
+    assert lib.fp8gemm_dense_ex(good, good, 0, good, good, 0, good, 4, 256, 256, 2, s) == b.ERR_FLAGS
+    assert lib.fp8gemm_dense_ex(good, good, 0, good, good, 0, good, 4, 256, 136, 1, s) == b.ERR_SHAPE
+    assert lib.fp8gemm_dense_ex(good, good, 0, good, good, 0, good, 0, 256, 256, 1, s) == b.OK
+    assert b.strerror(b.ERR_FLAGS).startswith("unknown flag")
 
 
 def test_problem_struct_layout():

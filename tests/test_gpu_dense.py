@@ -150,3 +150,34 @@ def synthetic_ops(M, N, K):
     Ao, sAo = oquant.quant_1x128_fast(Xf)
     Bo, sBo = oquant.quant_128x128_fast(Wf)
     return dev(Xf), dev(Bo), dev(sBo), ogemm.gemm_dense(Ao, sAo, Bo, sBo)
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (1, 7168, 2048),     # 5-CTA clusters
+    (64, 2048, 7168),    # 8-CTA clusters
+    (20, 1536, 7168),    # 12-CTA clusters
+    (17, 128, 16384),    # stream-K: the split-K workspace
+    (33, 1000, 1280),    # stream-K, ragged N tile
+])
+def test_read_only_weights_flag_in_a_chain(M, N, K):
+    """FP8GEMM_FLAG_B_READ_ONLY: the decode kernel stages its first weight
+    tiles before waiting for the kernel ahead of it.  Each GEMM's activations
+    are quantised by the kernel launched just before it (no host sync), so the
+    activation side must still wait; the weights are constant."""
+    from fp8_fine_grained_e4m3_gb300 import synthetic
+    b = _b()
+    _, W = synthetic.dense_operands(1, N, K, kind="decode", seed=N + K)
+    Bo, sBo = oquant.quant_128x128_fast(W) if K % 128 == 0 else oquant.quant_128x128(W)
+    tB, tsB = dev(Bo), dev(sBo)
+    outs, refs = [], []
+    for seed in (51, 52, 53):
+        X, _ = synthetic.dense_operands(M, 8, K, kind="decode", seed=seed)
+        tX = dev(X * np.float32(0.5)) * 2.0  # written by a kernel just before
+        A8, sA = b.fp8_quant_1x128(tX)
+        outs.append(b.fp8gemm_dense_ex(A8, sA, "e4m3", tB, tsB, "e4m3",
+                                       flags=b.FLAG_B_READ_ONLY))
+        Ao, sAo = oquant.quant_1x128_fast(X)
+        refs.append(ogemm.gemm_dense(Ao, sAo, Bo, sBo))
+    for got, ref in zip(outs, refs):
+        assert_close(host(got), ref, f"read-only weights {M}x{N}x{K}")
+    assert b.fp8gemm_get_device_status() == b.OK
