@@ -364,25 +364,28 @@ class Problem(ctypes.Structure):
     """One entry of the fp8gemm_grouped_table problem table (C layout)."""
     _fields_ = [("A", _P), ("sA", _P), ("B", _P), ("sB", _P), ("D", _P),
                 ("M", ctypes.c_int), ("N", ctypes.c_int), ("K", ctypes.c_int),
-                ("reserved", ctypes.c_int)]
+                ("formats", ctypes.c_int)]
 
 
 def problem_table(problems, out=None):
     """Device table for fp8gemm_grouped_table from (A, sA, B, sB, D) tensor
-    tuples: a uint8 CUDA tensor of len(problems) * sizeof(Problem) bytes
-    (written into `out` when given, e.g. to update a table a graph captured).
-    Every entry's tensors are checked against its (M, N, K) here, since the
-    kernel only sees the pointers."""
+    tuples, optionally extended by the operand formats, (A, sA, B, sB, D,
+    a_fmt, b_fmt) with "e4m3" / "e5m2": a uint8 CUDA tensor of
+    len(problems) * sizeof(Problem) bytes (written into `out` when given, e.g.
+    to update a table a graph captured).  Every entry's tensors are checked
+    against its (M, N, K) here, since the kernel only sees the pointers."""
     torch = _torch()
     arr = (Problem * len(problems))()
-    for e, (A, sA, B, sB, D) in zip(arr, problems):
-        A, B = _u8(A, "A"), _u8(B, "B")
+    for e, prob in zip(arr, problems):
+        A, sA, B, sB, D = prob[:5]
+        a_fmt, b_fmt = (prob[5], prob[6]) if len(prob) > 5 else ("e4m3", "e4m3")
+        A, B = _u8_fmt(A, a_fmt, "A"), _u8_fmt(B, b_fmt, "B")
         M, N, K = _dense_mnk(A, B)
         _shape_dense(A, _f32(sA, "sA"), B, _f32(sB, "sB"), D, M, N, K)
         e.A, e.sA, e.B = _dev(A, "A").data_ptr(), _dev(sA, "sA").data_ptr(), _dev(B, "B").data_ptr()
         e.sB, e.D = _dev(sB, "sB").data_ptr(), _dev(D, "D").data_ptr()
         e.M, e.N, e.K = M, N, K
-        e.reserved = 0
+        e.formats = _fmt(a_fmt) | (_fmt(b_fmt) << 8)
     host = torch.frombuffer(bytearray(bytes(arr)), dtype=torch.uint8)
     if out is None:
         return host.to("cuda")
@@ -392,7 +395,8 @@ def problem_table(problems, out=None):
 
 def fp8gemm_grouped_table(table, num_problems, max_M, stream=None):
     """Run every problem of a device table (see problem_table); max_M bounds
-    every entry's M (<= 64) and picks the kernel's padded width."""
+    every entry's M and picks the kernel's padded width (16, 32 or 64 rows;
+    larger entries are taken 64 rows at a time)."""
     if table.numel() < int(num_problems) * ctypes.sizeof(Problem):
         raise ValueError(f"table holds {table.numel()} bytes; {num_problems} entries need "
                          f"{int(num_problems) * ctypes.sizeof(Problem)}")

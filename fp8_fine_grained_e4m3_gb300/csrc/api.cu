@@ -350,7 +350,7 @@ int fp8gemm_dense_quant_a(const float* X, uint8_t* Q, float* sA, const uint8_t* 
 
 int fp8gemm_grouped_table(const fp8gemm_problem* problems, int num_problems, int max_M,
                           fp8gemm_stream_t stream) {
-  if (num_problems < 0 || max_M < 1 || max_M > kSmallM) return FP8GEMM_ERR_SHAPE;
+  if (num_problems < 0 || max_M < 1) return FP8GEMM_ERR_SHAPE;
   if (num_problems == 0) return FP8GEMM_OK;
   if (!problems) return FP8GEMM_ERR_NULL;
   if (reinterpret_cast<uintptr_t>(problems) & 7u) return FP8GEMM_ERR_ALIGN;

@@ -11,9 +11,13 @@
 //
 // Per problem p the arithmetic is fp8gemm_dense's (1x128 A scales, 128x128 B
 // scales, each K block contracted on the tensor cores and promoted into an
-// FP32 accumulator, BF16 out).  The decode layout of gemm_small_m.cu: swap-AB
-// (a 128-row weight tile is the MMA's M, the problem's M <= 64 rows padded to
-// MP its N), one TMEM partial per K block, promotion per output column.
+// FP32 accumulator, BF16 out), with each entry's own operand formats (e4m3 or
+// e5m2, "lpnh.cn/news/2822121" section 2.1).  The decode layout of
+// gemm_small_m.cu: swap-AB (a 128-row weight tile is the MMA's M, up to MP of
+// the problem's rows its N), one TMEM partial per K block, promotion per
+// output column.  A problem with more rows than MP is taken MP rows at a time:
+// its items are (N tile, row chunk), the chunks of one tile consecutive, so
+// CTAs running side by side share that weight tile through L2.
 //
 // What differs: no tensor maps (they would have to be rebuilt per problem on
 // the device), so four producer warps fill the 128-byte-swizzled operand
@@ -63,7 +67,10 @@ struct Prob {
   const uint8_t* B;
   const float* sB;
   __nv_bfloat16* D;
-  int M, N, K, Kb, tiles;
+  int M, N, K, Kb;
+  int chunks;  // row chunks of MP rows
+  int tiles;   // work items: N tiles x row chunks
+  int a_fmt, b_fmt;
   bool bad;
 };
 
@@ -71,7 +78,7 @@ __device__ __forceinline__ bool al16(const void* p) {
   return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
 }
 
-__device__ Prob load_problem(const fp8gemm_problem* tab, int p, int max_M) {
+__device__ Prob load_problem(const fp8gemm_problem* tab, int p, int max_M, int MP) {
   Prob r;
   const fp8gemm_problem* e = tab + p;
   r.A = reinterpret_cast<const uint8_t*>(__ldg(reinterpret_cast<const unsigned long long*>(&e->A)));
@@ -82,14 +89,19 @@ __device__ Prob load_problem(const fp8gemm_problem* tab, int p, int max_M) {
   r.M = __ldg(&e->M);
   r.N = __ldg(&e->N);
   r.K = __ldg(&e->K);
+  const int f = __ldg(&e->formats);
+  r.a_fmt = f & 0xff;
+  r.b_fmt = (f >> 8) & 0xff;
   const bool empty = r.M == 0 || r.N == 0;
   r.bad = r.M < 0 || r.N < 0 || r.M > max_M || r.K <= 0 || r.K % 16 != 0 ||
+          r.a_fmt > FP8GEMM_FMT_E5M2 || r.b_fmt > FP8GEMM_FMT_E5M2 || (f >> 16) != 0 ||
           (!empty && (!r.A || !r.sA || !r.B || !r.sB || !r.D || !al16(r.A) || !al16(r.B) ||
                       (reinterpret_cast<uintptr_t>(r.sA) & 3u) ||
                       (reinterpret_cast<uintptr_t>(r.sB) & 3u) ||
                       (reinterpret_cast<uintptr_t>(r.D) & 1u)));
   r.Kb = r.bad ? 0 : ceil_div(r.K, kBlockK);
-  r.tiles = (r.bad || empty) ? 0 : ceil_div(r.N, 128);
+  r.chunks = (r.bad || empty) ? 0 : ceil_div(r.M, MP);
+  r.tiles = (r.bad || empty) ? 0 : ceil_div(r.N, 128) * r.chunks;
   return r;
 }
 
@@ -97,7 +109,7 @@ __device__ Prob load_problem(const fp8gemm_problem* tab, int p, int max_M) {
 // j * gridDim.x over the concatenation of every problem's tiles.
 struct Walk {
   const fp8gemm_problem* tab;
-  int P, max_M;
+  int P, max_M, MP;
   int p = -1;
   long long first = 0;  // index of problem p's first item
   Prob cur;
@@ -105,13 +117,18 @@ struct Walk {
   __device__ bool seek(long long item) {
     if (p < 0) {
       p = 0;
-      if (P > 0) cur = load_problem(tab, 0, max_M);
+      if (P > 0) cur = load_problem(tab, 0, max_M, MP);
     }
     while (p < P && item >= first + cur.tiles) {
       first += cur.tiles;
-      if (++p < P) cur = load_problem(tab, p, max_M);
+      if (++p < P) cur = load_problem(tab, p, max_M, MP);
     }
     return p < P;
+  }
+  // This item's N tile and first row.
+  __device__ int tile(long long item) const { return int((item - first) / cur.chunks); }
+  __device__ int row0(long long item, int mp) const {
+    return int((item - first) % cur.chunks) * mp;
   }
 };
 
@@ -178,12 +195,13 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kCtasPerSm)
     // instruction; chunk c of tile row r lands at r * 128 + ((c ^ (r % 8)) * 16)
     const int c = lane % 8, r0 = lane / 8 + 4 * (warp - Cfg::kLoadWarp);
     constexpr int kRowStep = 4 * Cfg::kLoadWarps;
-    Walk w{tab, P, max_M};
+    Walk w{tab, P, max_M, MP};
     int i = 0;  // unit (K block) counter
     bool ok = true;
     for (long long item = blockIdx.x; ok && w.seek(item); item += gridDim.x) {
       const Prob& q = w.cur;
-      const int tile = int(item - w.first);
+      const int tile = w.tile(item);
+      const int m0 = w.row0(item, MP);
       for (int kb = 0; kb < q.Kb; ++kb, ++i) {
         const int s = i % kStages;
         if (!mbar_wait(&empty_bar[s], ((i / kStages) & 1) ^ 1, abort_flag, wait_ns)) {
@@ -203,8 +221,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kCtasPerSm)
         const uint32_t x_dst = smem_addr(smX + s * Cfg::kXBytes);
 #pragma unroll
         for (int r = r0; r < MP; r += kRowStep) {
-          const bool in = k_in && r < q.M;
-          const uint8_t* src = in ? q.A + size_t(r) * q.K + kb * kBlockK + c * 16 : q.A;
+          const bool in = k_in && m0 + r < q.M;
+          const uint8_t* src = in ? q.A + size_t(m0 + r) * q.K + kb * kBlockK + c * 16 : q.A;
           cp_async_16(x_dst + r * 128 + ((c ^ (r & 7)) << 4), src, in ? 16u : 0u);
         }
         cp_async_mbar_arrive(&full_bar[s]);  // arrives when this lane's copies land
@@ -214,13 +232,15 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kCtasPerSm)
   } else if (warp == Cfg::kMmaWarp) {
     // ------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_e4m3_f32(128, MP);
       const uint32_t w_base = smem_addr(smW);
       const uint32_t x_base = smem_addr(smX);
-      Walk w{tab, P, max_M};
+      Walk w{tab, P, max_M, MP};
       int i = 0;
       bool ok = true;
       for (long long item = blockIdx.x; ok && w.seek(item); item += gridDim.x) {
+        // swap-AB: the MMA's A operand is the weights (the problem's B)
+        const uint32_t idesc =
+            idesc_f8_f32(128, MP, uint32_t(w.cur.b_fmt), uint32_t(w.cur.a_fmt));
         for (int kb = 0; kb < w.cur.Kb; ++kb, ++i) {
           const int s = i % kStages;
           const int buf = i % NB;
@@ -264,13 +284,15 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kCtasPerSm)
     };
     if (t == 0) {  // report entries that break the contract (once per launch)
       for (int p = blockIdx.x; p < P; p += gridDim.x)
-        if (load_problem(tab, p, max_M).bad) raise_status(status, FP8GEMM_ERR_DEVICE_STATUS);
+        if (load_problem(tab, p, max_M, MP).bad) raise_status(status, FP8GEMM_ERR_DEVICE_STATUS);
     }
-    Walk w{tab, P, max_M};
+    Walk w{tab, P, max_M, MP};
     int i = 0;
     for (long long item = blockIdx.x; ok && w.seek(item); item += gridDim.x) {
       const Prob q = w.cur;
-      const int tile = int(item - w.first);
+      const int tile = w.tile(item);
+      const int m0 = w.row0(item, MP);
+      const int rows = min(MP, q.M - m0);  // rows of this chunk
       float acc[MP];
 #pragma unroll
       for (int j = 0; j < MP; ++j) acc[j] = 0.f;
@@ -281,7 +303,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kCtasPerSm)
           if (!group_sync()) { fail(); ok = false; break; }
           for (int idx = t; idx < MP * nkb; idx += 128) {
             const int j = idx / nkb, b = idx % nkb;
-            sa_s[b * MP + j] = j < q.M ? __ldg(q.sA + size_t(j) * q.Kb + kb + b) : 0.f;
+            sa_s[b * MP + j] = j < rows ? __ldg(q.sA + size_t(m0 + j) * q.Kb + kb + b) : 0.f;
           }
           if (t < nkb) sb_s[t] = __ldg(q.sB + size_t(tile) * q.Kb + kb + t);
           if (!group_sync()) { fail(); ok = false; break; }
@@ -328,7 +350,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kCtasPerSm)
       if (n < q.N) {
 #pragma unroll
         for (int j = 0; j < MP; ++j)
-          if (j < q.M) q.D[size_t(j) * q.N + n] = __float2bfloat16_rn(acc[j]);
+          if (j < rows) q.D[size_t(m0 + j) * q.N + n] = __float2bfloat16_rn(acc[j]);
       }
     }
   }

@@ -266,22 +266,28 @@ int fp8gemm_grouped_masked_fmt(const uint8_t* A, const float* sA, int a_fmt, con
  * sizes) is read on the device when the kernel runs, so it may be rewritten
  * between replays of a graph that captured this call.
  *
- * Per entry p (e4m3 operands, the layouts and arithmetic of fp8gemm_dense):
+ * Per entry p (the layouts and arithmetic of fp8gemm_dense_fmt):
  *   A u8 [M, K], sA f32 [M, ceil(K/128)], B u8 [N, K],
  *   sB f32 [ceil(N/128), ceil(K/128)], D bf16 [M, N] (written in full)
- * with 0 <= M <= max_M <= 64, N >= 0, K > 0 and K % 16 == 0, A and B 16-byte
- * aligned, sA and sB 4-byte, D 2-byte.  An entry with M = 0 or N = 0 is
+ * with 0 <= M <= max_M, N >= 0, K > 0 and K % 16 == 0, A and B 16-byte
+ * aligned, sA and sB 4-byte, D 2-byte, and `formats` = a_fmt | (b_fmt << 8)
+ * (FP8GEMM_FMT_* each; 0 means e4m3 x e4m3).  An entry with M = 0 or N = 0 is
  * skipped.  An entry that breaks these rules is skipped and sets
  * FP8GEMM_ERR_DEVICE_STATUS (read it with fp8gemm_get_device_status).
  * Entries must not write overlapping D.
  *
- * Each (entry, 128-column tile) runs its whole K range on one CTA; there is
- * no split-K across CTAs here, so a batch with few tiles in total leaves SMs
- * idle (fp8gemm_dense splits K for a single problem).
+ * The kernel is built for decode-sized problems (the padded width is 16, 32
+ * or 64 rows, chosen from max_M).  An entry with more rows is processed that
+ * many rows at a time -- each 64-row chunk streams the entry's weight tiles
+ * again, mostly from L2 -- so large-M problems are served correctly but
+ * fp8gemm_dense is the faster call for them.  Each (entry, 128-column tile,
+ * row chunk) runs its whole K range on one CTA; there is no split-K across
+ * CTAs here, so a batch with few tiles in total leaves SMs idle
+ * (fp8gemm_dense splits K for a single problem).
  *
  *   problems  device array of num_problems entries, 8-byte aligned
- * Host-side errors: FP8GEMM_ERR_SHAPE (num_problems < 0, max_M outside
- * 1..64), FP8GEMM_ERR_NULL, FP8GEMM_ERR_ALIGN.
+ * Host-side errors: FP8GEMM_ERR_SHAPE (num_problems < 0, max_M < 1),
+ * FP8GEMM_ERR_NULL, FP8GEMM_ERR_ALIGN.
  */
 typedef struct fp8gemm_problem {
   const uint8_t* A;
@@ -290,7 +296,7 @@ typedef struct fp8gemm_problem {
   const float* sB;
   void* D;
   int M, N, K;
-  int reserved; /* set to 0 */
+  int formats; /* a_fmt | (b_fmt << 8); 0 = e4m3 x e4m3 */
 } fp8gemm_problem;
 
 int fp8gemm_grouped_table(const fp8gemm_problem* problems, int num_problems, int max_M,

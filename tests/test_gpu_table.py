@@ -1,7 +1,8 @@
-"""fp8gemm_grouped_table: many decode-sized problems from a device-resident
-table, against the oracle; a captured CUDA graph replayed after the table was
-rewritten with other shapes and pointers; entries that are empty or break the
-contract."""
+"""fp8gemm_grouped_table: many problems from a device-resident table, against
+the oracle -- decode-sized ones, entries of a few hundred rows (taken 64 rows
+at a time), e5m2 and mixed-format entries; a captured CUDA graph replayed
+after the table was rewritten with other shapes and pointers; entries that
+are empty or break the contract."""
 
 import numpy as np
 import pytest
@@ -17,14 +18,14 @@ def _b():
     return binding
 
 
-def _problem(M, N, K, seed):
+def _problem(M, N, K, seed, a_fmt="e4m3", b_fmt="e4m3"):
     import torch
     X, W = synthetic.dense_operands(M, N, K, kind="decode", seed=seed)
-    A, sA = oquant.quant_1x128_fast(X)
-    B, sB = quant_weights(W)
-    ref = ogemm.gemm_dense(A, sA, B, sB)
+    A, sA = oquant.quant_1x128(X, fmt=a_fmt) if a_fmt != "e4m3" else oquant.quant_1x128_fast(X)
+    B, sB = oquant.quant_128x128(W, fmt=b_fmt) if b_fmt != "e4m3" else quant_weights(W)
+    ref = ogemm.gemm_dense(A, sA, B, sB, a_fmt=a_fmt, b_fmt=b_fmt)
     D = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
-    return (dev(A), dev(sA), dev(B), dev(sB), D), ref
+    return (dev(A), dev(sA), dev(B), dev(sB), D, a_fmt, b_fmt), ref
 
 
 SHAPES = [(1, 2048, 7168), (5, 300, 400), (16, 7168, 2048), (33, 777, 1024), (64, 128, 256),
@@ -41,8 +42,35 @@ def test_table_matches_oracle(max_M, shapes):
     probs, refs = zip(*[_problem(M, N, K, seed=i + M) for i, (M, N, K) in enumerate(shapes)])
     table = b.problem_table(probs)
     b.fp8gemm_grouped_table(table, len(probs), max_M)
-    for (_, _, _, _, D), ref, shp in zip(probs, refs, shapes):
-        assert_close(host(D), ref, f"table problem {shp}")
+    for prob, ref, shp in zip(probs, refs, shapes):
+        assert_close(host(prob[4]), ref, f"table problem {shp}")
+    assert b.fp8gemm_get_device_status() == b.OK
+
+
+@pytest.mark.parametrize("max_M,shapes", [
+    # entries above 64 rows: taken 64 rows at a time (last chunk partial)
+    (300, [(300, 1024, 512), (65, 640, 2048), (1, 7168, 2048), (200, 384, 1040), (128, 256, 256)]),
+    (129, [(129, 2048, 1024), (64, 300, 400), (100, 129, 4096)]),
+])
+def test_table_entries_above_64_rows(max_M, shapes):
+    b = _b()
+    probs, refs = zip(*[_problem(M, N, K, seed=60 + i) for i, (M, N, K) in enumerate(shapes)])
+    b.fp8gemm_grouped_table(b.problem_table(probs), len(probs), max_M)
+    for prob, ref, shp in zip(probs, refs, shapes):
+        assert_close(host(prob[4]), ref, f"table problem {shp}")
+    assert b.fp8gemm_get_device_status() == b.OK
+
+
+def test_table_with_e5m2_and_mixed_entries():
+    b = _b()
+    spec = [((16, 640, 1024), "e5m2", "e4m3"), ((5, 300, 400), "e4m3", "e5m2"),
+            ((33, 777, 2048), "e5m2", "e5m2"), ((90, 512, 272), "e5m2", "e4m3"),
+            ((8, 2048, 1024), "e4m3", "e4m3")]
+    probs, refs = zip(*[_problem(M, N, K, seed=80 + i, a_fmt=af, b_fmt=bf)
+                        for i, ((M, N, K), af, bf) in enumerate(spec)])
+    b.fp8gemm_grouped_table(b.problem_table(probs), len(probs), 90)
+    for prob, ref, (shp, af, bf) in zip(probs, refs, spec):
+        assert_close(host(prob[4]), ref, f"table problem {shp} {af} x {bf}")
     assert b.fp8gemm_get_device_status() == b.OK
 
 
@@ -58,7 +86,7 @@ def test_graph_replay_with_rewritten_table():
     table = torch.zeros(P * 56, dtype=torch.uint8, device="cuda")
     # the first set padded with an empty entry (M = 0) to the captured count
     empty = (first[0][0][0][:0], first[0][0][1][:0], first[0][0][2], first[0][0][3],
-             first[0][0][4][:0])
+             first[0][0][4][:0])  # M = 0
     b.problem_table([p for p, _ in first] + [empty], out=table)
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
@@ -87,18 +115,19 @@ def test_bad_and_empty_entries():
     good, ref = _problem(8, 512, 1024, seed=7)
     other, ref2 = _problem(3, 256, 256, seed=8)
     import ctypes
-    arr = (b.Problem * 4)()
-    for e, (A, sA, B, sB, D) in zip(arr, [good, other, good, good]):
+    arr = (b.Problem * 5)()
+    for e, (A, sA, B, sB, D, _, _) in zip(arr, [good, other, good, good, good]):
         e.A, e.sA, e.B, e.sB, e.D = (A.data_ptr(), sA.data_ptr(), B.data_ptr(), sB.data_ptr(),
                                      D.data_ptr())
         e.M, e.K = A.shape
         e.N = B.shape[0]
     arr[2].M = 65            # beyond max_M: skipped, status raised
     arr[3].A = arr[3].A + 4  # misaligned A: skipped, status raised
+    arr[4].formats = 2       # unknown operand format: skipped, status raised
     bad_D = torch.full((8, 512), 7.0, dtype=torch.bfloat16, device="cuda")
-    arr[2].D = arr[3].D = bad_D.data_ptr()
+    arr[2].D = arr[3].D = arr[4].D = bad_D.data_ptr()
     table = torch.frombuffer(bytearray(bytes(arr)), dtype=torch.uint8).cuda()
-    b.fp8gemm_grouped_table(table, 4, 64)
+    b.fp8gemm_grouped_table(table, 5, 64)
     assert b.fp8gemm_get_device_status() == b.ERR_DEVICE_STATUS
     assert_close(host(good[4]), ref, "good entry beside bad ones")
     assert_close(host(other[4]), ref2, "second good entry")
