@@ -151,7 +151,8 @@ int finish(cudaError_t e, int nlaunch) {
 // counters must start at 0 and are left at 0).  Slot kWsQuantA: quantised
 // activations of fp8gemm_dense_quant_a at large M -- a separate buffer, so
 // those bytes never land on the counters.
-enum { kWsSplitK = 0, kWsQuantA = 1 };
+// Slot kWsTable: the stream-K partials and counters of the problem-table GEMM.
+enum { kWsSplitK = 0, kWsQuantA = 1, kWsTable = 2 };
 
 int workspace_for(cudaStream_t s, size_t bytes, void** out, int slot = kWsSplitK) {
   int dev = 0;
@@ -356,7 +357,10 @@ int fp8gemm_grouped_table(const fp8gemm_problem* problems, int num_problems, int
   if (reinterpret_cast<uintptr_t>(problems) & 7u) return FP8GEMM_ERR_ALIGN;
   LaunchCtx c;
   if (int r = ctx_for(stream, &c)) return r;
-  return finish(launch_gemm_table(c, problems, num_problems, max_M), 1);
+  const size_t bytes = table_workspace_bytes(c, max_M);
+  void* ws = nullptr;
+  if (int r = workspace_for(stream, bytes, &ws, kWsTable)) return r;
+  return finish(launch_gemm_table(c, problems, num_problems, max_M, ws, bytes), 1);
 }
 
 static bool valid_fmt(int f) { return f == FP8GEMM_FMT_E4M3 || f == FP8GEMM_FMT_E5M2; }

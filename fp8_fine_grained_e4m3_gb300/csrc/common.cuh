@@ -78,8 +78,12 @@ bool small_m_uses_workspace(const LaunchCtx& c, const GemmArgs& a);
 cudaError_t launch_gemm_small_m_any(const LaunchCtx& c, const GemmArgs& a, void* ws,
                                     size_t ws_bytes);
 
-// Many decode-sized problems from a device-resident table (gemm_table.cu).
-cudaError_t launch_gemm_table(const LaunchCtx& c, const fp8gemm_problem* tab, int P, int max_M);
+// Many decode-sized problems from a device-resident table (gemm_table.cu),
+// K split over the CTAs (stream-K) through a zeroed workspace of
+// table_workspace_bytes bytes whose counters each launch leaves at zero.
+size_t table_workspace_bytes(const LaunchCtx& c, int max_M);
+cudaError_t launch_gemm_table(const LaunchCtx& c, const fp8gemm_problem* tab, int P, int max_M,
+                              void* ws, size_t ws_bytes);
 
 // Fills `c` for the current device and `stream` (SM count, status word);
 // returns an fp8gemm_status code.  Defined in api.cu.

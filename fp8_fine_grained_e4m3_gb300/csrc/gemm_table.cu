@@ -26,9 +26,17 @@
 // barrier when that lane's copies have landed; the MMA thread fences the
 // generic proxy against the async one before the tensor cores read the stage.
 // (One producer warp issued too few copies to keep a stage's 16 KB moving:
-// 215 us against 116 us with four, on 16 decode problems of 4096x7168.)  Work
-// items are (problem, N tile) pairs with the whole K range, taken by
-// persistent CTAs in a fixed order that every role walks identically.
+// 215 us against 116 us with four, on 16 decode problems of 4096x7168.)
+//
+// Work division: stream-K.  The (item, K block) units of all problems, in
+// table order, are dealt out evenly over the persistent CTAs -- whole items
+// over a fixed grid leave the last round mostly idle when there are few
+// items per CTA ("news.rkmt.cn/news/5092" section 4.2: size the work to the
+// SM count).  A CTA whose range begins or ends inside an item leaves its FP32
+// partial in a workspace slot; the last contributor to finish the item (one
+// acquire-release atomic per contributor, on a counter owned by the item's
+// first CTA) sums every partial in CTA order -- deterministic -- writes BF16
+// and resets the counter.  Every role walks the CTA's unit range identically.
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -54,7 +62,8 @@ struct TabCfg {
   static constexpr int kAuxBytes = kBarBytes + kScaleKb * (MP + 4) * 4;
   static constexpr size_t kSmemBytes =
       1024 + size_t(kStages) * (kWBytes + kXBytes) + kAuxBytes;
-  static_assert((2 * kStages + 2 * kTmemBufs + 4) * 8 + 16 <= kBarBytes, "barrier area");
+  // barriers, then TMEM holder, abort and last flags, and the CTA's range
+  static_assert((2 * kStages + 2 * kTmemBufs + 2) * 8 + 16 + 4 * 8 <= kBarBytes, "barrier area");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
   static_assert(kCtasPerSm == 1 || kSmemBytes <= 113 * 1024, "two CTAs per SM");
 };
@@ -107,35 +116,120 @@ __device__ Prob load_problem(const fp8gemm_problem* tab, int p, int max_M, int M
 
 // The (problem, N tile) items of this CTA, in order: item = blockIdx.x +
 // j * gridDim.x over the concatenation of every problem's tiles.
+// How the table's work is dealt out, the same choice in every CTA: whole
+// items round-robin (r[2] = 0), unless that leaves the grid less than 70 %
+// busy (fewer items than CTAs, or a last round mostly empty); then the units
+// themselves are split evenly (stream-K) over r[2] CTAs -- at most one per
+// unit, so that every CTA taking part has a non-empty range -- this CTA's
+// being [r[0], r[1]).  r[3]: the table's units.
+__device__ void table_range(const fp8gemm_problem* tab, int P, int max_M, int MP, int c, int G,
+                            long long r[4]) {
+  long long U = 0, I = 0;
+  for (int p = 0; p < P; ++p) {
+    const Prob q = load_problem(tab, p, max_M, MP);
+    U += (long long)q.tiles * q.Kb;
+    I += q.tiles;
+  }
+  r[0] = r[1] = r[2] = 0;
+  r[3] = U;
+  if (U == 0 || U > 0x7fffffffLL) return;  // more units than 32-bit indices: nothing to do
+  const long long rounds = (I + G - 1) / G;
+  if (10 * I < 7LL * G * rounds) {  // stream-K
+    const long long active = U < G ? U : G;
+    r[2] = active;
+    if (c < active) {
+      r[0] = c * U / active;
+      r[1] = (c + 1) * U / active;
+    }
+    return;
+  }
+}
+
+// A CTA's units [begin(c), begin(c + 1)) and the CTA holding unit u.
+struct Split {
+  long long U;
+  int G;
+  __device__ int begin(int c) const { return int((long long)c * U / G); }
+  __device__ int cta_of(int u) const { return int(((long long)(u + 1) * G - 1) / U); }
+};
+
+// One item's share of a CTA's unit range: K blocks [kb0, kb1) of the item
+// whose first unit is item_u0 (rows m0.., N tile `tile` of problem cur).
+struct Seg {
+  int tile, m0, kb0, kb1;
+  int item_u0;
+};
+
+// Walks the problems in table order by unit (or item) index.
 struct Walk {
   const fp8gemm_problem* tab;
   int P, max_M, MP;
   int p = -1;
-  long long first = 0;  // index of problem p's first item
+  int first = 0;       // problem p's first unit (the table's units fit in int)
+  int first_item = 0;  // and first item
   Prob cur;
-  // Moves to the problem holding `item`; false past the last one.
-  __device__ bool seek(long long item) {
+  __device__ void advance() {
+    first += cur.tiles * cur.Kb;
+    first_item += cur.tiles;
+    if (++p < P) cur = load_problem(tab, p, max_M, MP);
+  }
+  __device__ void start() {
     if (p < 0) {
       p = 0;
       if (P > 0) cur = load_problem(tab, 0, max_M, MP);
     }
-    while (p < P && item >= first + cur.tiles) {
-      first += cur.tiles;
-      if (++p < P) cur = load_problem(tab, p, max_M, MP);
-    }
+  }
+  // Moves to the problem holding unit u; false past the last one.
+  __device__ bool seek(int u) {
+    start();
+    while (p < P && u >= first + cur.tiles * cur.Kb) advance();
     return p < P;
   }
-  // This item's N tile and first row.
-  __device__ int tile(long long item) const { return int((item - first) / cur.chunks); }
-  __device__ int row0(long long item, int mp) const {
-    return int((item - first) % cur.chunks) * mp;
+  // Moves to the problem holding item i; false past the last one.
+  __device__ bool seek_item(int i) {
+    start();
+    while (p < P && i >= first_item + cur.tiles) advance();
+    return p < P;
+  }
+  // The segment that starts at unit u and ends at `end` or the item's end.
+  __device__ __forceinline__ Seg segment(int u, int end) const {
+    const int rel = u - first;
+    const int item = rel / cur.Kb;
+    Seg g;
+    g.kb0 = rel - item * cur.Kb;
+    g.kb1 = min(cur.Kb, g.kb0 + (end - u));
+    g.tile = item / cur.chunks;
+    g.m0 = (item % cur.chunks) * MP;
+    g.item_u0 = first + item * cur.Kb;
+    return g;
   }
 };
+
+// A CTA's next segment, k counting them: whole items blockIdx.x,
+// + gridDim.x, ... (rng[2] == 0), or (stream-K) the next piece of the CTA's
+// unit range [rng[0], rng[1]), whose first piece is k == 0.  Every role walks
+// the same sequence.
+__device__ __forceinline__ bool next_seg(Walk& w, const volatile long long* rng, int& k, int& u,
+                                         Seg& g) {
+  if (rng[2] == 0) {
+    const int item = int(blockIdx.x) + k * int(gridDim.x);
+    if (!w.seek_item(item)) return false;
+    const int iu = w.first + (item - w.first_item) * w.cur.Kb;
+    g = w.segment(iu, iu + w.cur.Kb);
+  } else {
+    if (k == 0) u = int(rng[0]);
+    if (u >= int(rng[1]) || !w.seek(u)) return false;
+    g = w.segment(u, int(rng[1]));
+    u += g.kb1 - g.kb0;
+  }
+  ++k;
+  return true;
+}
 
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kCtasPerSm)
     gemm_table_kernel(const fp8gemm_problem* __restrict__ tab, int P, int max_M, int* status,
-                      unsigned long long wait_ns) {
+                      unsigned long long wait_ns, float* ws_partials, int* ws_counters) {
   constexpr int MP = Cfg::MP;
   constexpr int kStages = Cfg::kStages;
   constexpr int NB = Cfg::kTmemBufs;
@@ -154,6 +248,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kCtasPerSm)
   uint64_t* group_bar = drain_bar + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(group_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_holder + 2);
+  long long* range_s = reinterpret_cast<long long*>(tmem_holder + 4);  // [4]
   float* sa_s = reinterpret_cast<float*>(aux + Cfg::kBarBytes);
   float* sb_s = sa_s + Cfg::kScaleKb * MP;
 
@@ -188,6 +284,16 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kCtasPerSm)
     raise_status(status, FP8GEMM_ERR_TIMEOUT);
   };
   griddep_wait();  // the table and the operands belong to the stream's order
+  if (threadIdx.x == 0)
+    table_range(tab, P, max_M, MP, int(blockIdx.x), int(gridDim.x), const_cast<long long*>(range_s));
+  __syncthreads();
+  // the range stays in shared memory (read where used): registers are short
+  // in the two-CTAs-per-SM configuration
+  const volatile long long* rng = range_s;
+  // stream-K: an item's contributors are exactly the CTAs from its first to
+  // its last unit's (every one of them has a non-empty range)
+  auto sk = [&]() { return Split{rng[3], int(rng[2])}; };
+
 
   if (warp >= Cfg::kLoadWarp && warp < Cfg::kLoadWarp + Cfg::kLoadWarps) {
     // ------------------------------------------------------ producer
@@ -198,11 +304,12 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kCtasPerSm)
     Walk w{tab, P, max_M, MP};
     int i = 0;  // unit (K block) counter
     bool ok = true;
-    for (long long item = blockIdx.x; ok && w.seek(item); item += gridDim.x) {
+    int k = 0, u = 0;
+    Seg g;
+    while (ok && next_seg(w, rng, k, u, g)) {
       const Prob& q = w.cur;
-      const int tile = w.tile(item);
-      const int m0 = w.row0(item, MP);
-      for (int kb = 0; kb < q.Kb; ++kb, ++i) {
+      const int tile = g.tile, m0 = g.m0;
+      for (int kb = g.kb0; kb < g.kb1; ++kb, ++i) {
         const int s = i % kStages;
         if (!mbar_wait(&empty_bar[s], ((i / kStages) & 1) ^ 1, abort_flag, wait_ns)) {
           fail();
@@ -237,11 +344,13 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kCtasPerSm)
       Walk w{tab, P, max_M, MP};
       int i = 0;
       bool ok = true;
-      for (long long item = blockIdx.x; ok && w.seek(item); item += gridDim.x) {
+      int k = 0, u = 0;
+      Seg g;
+      while (ok && next_seg(w, rng, k, u, g)) {
         // swap-AB: the MMA's A operand is the weights (the problem's B)
         const uint32_t idesc =
             idesc_f8_f32(128, MP, uint32_t(w.cur.b_fmt), uint32_t(w.cur.a_fmt));
-        for (int kb = 0; kb < w.cur.Kb; ++kb, ++i) {
+        for (int kb = g.kb0; kb < g.kb1; ++kb, ++i) {
           const int s = i % kStages;
           const int buf = i % NB;
           if (!mbar_wait(&tempty_bar[buf], ((i / NB) & 1) ^ 1, abort_flag, wait_ns) ||
@@ -288,18 +397,20 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kCtasPerSm)
     }
     Walk w{tab, P, max_M, MP};
     int i = 0;
-    for (long long item = blockIdx.x; ok && w.seek(item); item += gridDim.x) {
-      const Prob q = w.cur;
-      const int tile = w.tile(item);
-      const int m0 = w.row0(item, MP);
+    int k = 0, u = 0;
+    Seg g;
+    while (ok && next_seg(w, rng, k, u, g)) {
+      const Prob& q = w.cur;  // the walk does not move until the next segment
+      const bool seg_first = k == 1;  // this CTA's first segment
+      const int tile = g.tile, m0 = g.m0;
       const int rows = min(MP, q.M - m0);  // rows of this chunk
       float acc[MP];
 #pragma unroll
       for (int j = 0; j < MP; ++j) acc[j] = 0.f;
-      for (int kb = 0; kb < q.Kb; ++kb, ++i) {
-        const int qq = kb % Cfg::kScaleKb;
+      for (int kb = g.kb0; kb < g.kb1; ++kb, ++i) {
+        const int qq = (kb - g.kb0) % Cfg::kScaleKb;
         if (qq == 0) {  // stage the next batch of scales
-          const int nkb = min(Cfg::kScaleKb, q.Kb - kb);
+          const int nkb = min(Cfg::kScaleKb, g.kb1 - kb);
           if (!group_sync()) { fail(); ok = false; break; }
           for (int idx = t; idx < MP * nkb; idx += 128) {
             const int j = idx / nkb, b = idx % nkb;
@@ -346,8 +457,44 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kCtasPerSm)
         }
       }
       if (!ok) break;
+      bool write = true;
+      if (!(g.kb0 == 0 && g.kb1 == q.Kb)) {
+        // part of an item: publish this CTA's partial (the item's real rows);
+        // the last contributor sums them all in CTA order
+        float* mine = ws_partials + size_t(2 * blockIdx.x + (seg_first ? 0 : 1)) * MP * 128;
+#pragma unroll
+        for (int j = 0; j < MP; ++j)
+          if (j < rows) mine[j * 128 + t] = acc[j];
+        if (!group_sync()) { fail(); ok = false; break; }
+        const int c_first = sk().cta_of(g.item_u0);
+        const int c_last = sk().cta_of(g.item_u0 + q.Kb - 1);
+        if (t == 0) {
+          // release this CTA's partial (ordered before by the group barrier),
+          // acquire those of the contributors that arrived earlier
+          const int prev = atomic_add_acq_rel_gpu(ws_counters + c_first, 1);
+          const int is_last = prev == c_last - c_first;
+          if (is_last) ws_counters[c_first] = 0;  // ready for the next launch
+          *last_flag = is_last;
+        }
+        if (!group_sync()) { fail(); ok = false; break; }
+        write = *last_flag != 0;
+        if (!group_sync()) { fail(); ok = false; break; }  // last_flag is reused
+        if (write) {
+#pragma unroll
+          for (int j = 0; j < MP; ++j) acc[j] = 0.f;
+          for (int c = c_first; c <= c_last; ++c) {
+            // contributor c's slot: its first segment unless the item began
+            // after the start of c's range
+            const int cs = (c > c_first || g.item_u0 == sk().begin(c)) ? 2 * c : 2 * c + 1;
+            const float* pp = ws_partials + size_t(cs) * MP * 128;
+#pragma unroll
+            for (int j = 0; j < MP; ++j)
+              if (j < rows) acc[j] += __ldcg(pp + j * 128 + t);
+          }
+        }
+      }
       const int n = tile * 128 + t;
-      if (n < q.N) {
+      if (write && n < q.N) {
 #pragma unroll
         for (int j = 0; j < MP; ++j)
           if (j < rows) q.D[size_t(m0 + j) * q.N + n] = __float2bfloat16_rn(acc[j]);
@@ -362,8 +509,27 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kCtasPerSm)
   }
 }
 
+// Workspace layout, the same for every configuration so that one per-stream
+// buffer can serve them all: the counters (one per CTA of the largest grid,
+// two CTAs per SM) first, then the partial slots.  The counters are zero
+// between launches; partial slots are written before they are read.
+size_t counter_bytes(const LaunchCtx& c) {
+  return (size_t(c.num_sms) * 2 * sizeof(int) + 255) / 256 * 256;
+}
+
 template <class Cfg>
-cudaError_t run(const LaunchCtx& c, const fp8gemm_problem* tab, int P, int max_M) {
+size_t workspace_bytes(const LaunchCtx& c) {
+  const size_t grid = size_t(c.num_sms) * Cfg::kCtasPerSm;
+  return counter_bytes(c) + 2 * grid * Cfg::MP * 128 * sizeof(float);
+}
+
+template <class Cfg>
+cudaError_t run(const LaunchCtx& c, const fp8gemm_problem* tab, int P, int max_M, void* ws,
+                size_t ws_bytes) {
+  static_assert(Cfg::kCtasPerSm <= 2, "counter region");
+  if (ws_bytes < workspace_bytes<Cfg>(c)) return cudaErrorInvalidValue;
+  int* counters = static_cast<int*>(ws);
+  float* partials = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + counter_bytes(c));
   static unsigned long long attr_done = 0;  // one bit per device
   int dev = 0;
   cudaGetDevice(&dev);
@@ -385,15 +551,22 @@ cudaError_t run(const LaunchCtx& c, const fp8gemm_problem* tab, int P, int max_M
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, gemm_table_kernel<Cfg>, tab, P, max_M, c.status,
-                            wait_limit_ns());
+                            wait_limit_ns(), partials, counters);
 }
 
 }  // namespace
 
-cudaError_t launch_gemm_table(const LaunchCtx& c, const fp8gemm_problem* tab, int P, int max_M) {
-  if (max_M <= 16) return run<TabCfg<16>>(c, tab, P, max_M);
-  if (max_M <= 32) return run<TabCfg<32>>(c, tab, P, max_M);
-  return run<TabCfg<64>>(c, tab, P, max_M);
+size_t table_workspace_bytes(const LaunchCtx& c, int max_M) {
+  if (max_M <= 16) return workspace_bytes<TabCfg<16>>(c);
+  if (max_M <= 32) return workspace_bytes<TabCfg<32>>(c);
+  return workspace_bytes<TabCfg<64>>(c);
+}
+
+cudaError_t launch_gemm_table(const LaunchCtx& c, const fp8gemm_problem* tab, int P, int max_M,
+                              void* ws, size_t ws_bytes) {
+  if (max_M <= 16) return run<TabCfg<16>>(c, tab, P, max_M, ws, ws_bytes);
+  if (max_M <= 32) return run<TabCfg<32>>(c, tab, P, max_M, ws, ws_bytes);
+  return run<TabCfg<64>>(c, tab, P, max_M, ws, ws_bytes);
 }
 
 }  // namespace fp8gemm

@@ -280,10 +280,13 @@ int fp8gemm_grouped_masked_fmt(const uint8_t* A, const float* sA, int a_fmt, con
  * or 64 rows, chosen from max_M).  An entry with more rows is processed that
  * many rows at a time -- each 64-row chunk streams the entry's weight tiles
  * again, mostly from L2 -- so large-M problems are served correctly but
- * fp8gemm_dense is the faster call for them.  Each (entry, 128-column tile,
- * row chunk) runs its whole K range on one CTA; there is no split-K across
- * CTAs here, so a batch with few tiles in total leaves SMs idle
- * (fp8gemm_dense splits K for a single problem).
+ * fp8gemm_dense is the faster call for them.  The (entry, 128-column tile,
+ * row chunk, K block) units of the whole table are divided evenly over the
+ * CTAs (stream-K): an item whose K range is shared by several CTAs is summed
+ * from their FP32 partials in a fixed order, through a per-(device, stream)
+ * workspace that the library allocates and zeroes on the first call on the
+ * stream (a few MB; not during stream capture, see the conventions above), so
+ * results are deterministic for a given table and launch configuration.
  *
  *   problems  device array of num_problems entries, 8-byte aligned
  * Host-side errors: FP8GEMM_ERR_SHAPE (num_problems < 0, max_M < 1),

@@ -133,3 +133,23 @@ def test_bad_and_empty_entries():
     assert_close(host(other[4]), ref2, "second good entry")
     assert bool((bad_D == 7.0).all())  # skipped entries write nothing
     assert b.fp8gemm_get_device_status() == b.OK  # the read cleared it
+
+
+def test_table_few_items_split_along_k():
+    """Fewer (entry, tile) items than CTAs: the kernel splits their K ranges
+    over the CTAs (stream-K) and sums the partials in a fixed order, so the
+    result matches the oracle and repeats bit for bit."""
+    b = _b()
+    shapes = [(3, 256, 7168), (16, 128, 16384), (1, 384, 2048), (40, 128, 1040)]
+    probs, refs = zip(*[_problem(M, N, K, seed=90 + i) for i, (M, N, K) in enumerate(shapes)])
+    table = b.problem_table(probs)
+    b.fp8gemm_grouped_table(table, len(probs), 64)
+    first = [host(p[4]).copy() for p in probs]
+    for got, ref, shp in zip(first, refs, shapes):
+        assert_close(got, ref, f"split table problem {shp}")
+    for p in probs:
+        p[4].fill_(float("nan"))
+    b.fp8gemm_grouped_table(table, len(probs), 64)
+    for p, f in zip(probs, first):
+        assert np.array_equal(host(p[4]), f)
+    assert b.fp8gemm_get_device_status() == b.OK
