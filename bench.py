@@ -466,7 +466,15 @@ def measure_configs(peaks, dev):
             r = _roof(2 * M * N * K, gemm_bytes(M, N, K), ms_ro, peaks)
             r["timing"] = "CUDA graph, 24 rotating weight copies; weights declared read-only"
             res[f"decode_ro_{M}x{N}x{K}"] = r
-            del copies, fns, fns_q, fns_ro, X
+            fns_qro = [(lambda Bc=Bc, sBc=sBc: b.fp8gemm_dense_quant_a(X, Bc, sBc, D=D,
+                                                                       flags=b.FLAG_B_READ_ONLY))
+                       for Bc, sBc in copies]
+            ms_qro = time_graph(fns_qro, reps=4)
+            r = _roof(2 * M * N * K, nb, ms_qro, peaks)
+            r["timing"] = ("CUDA graph, 24 rotating weight copies; quantiser + GEMM, weights "
+                           "declared read-only (staged while the quantiser runs)")
+            res[f"decode_quant_a_ro_{M}x{N}x{K}"] = r
+            del copies, fns, fns_q, fns_ro, fns_qro, X
 
     # mixed formats: e5m2 A (a gradient) against e4m3 B, large and decode shapes
     for (M, N, K) in ((4096, 7168, 16384), (16, 7168, 2048)):

@@ -50,6 +50,7 @@ SIGNATURES = [
      [_P, _P, _I, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P]),
     ("fp8gemm_grouped_masked_fmt", _I, [_P, _P, _I, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P]),
     ("fp8gemm_dense_quant_a", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
+    ("fp8gemm_dense_quant_a_ex", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, ctypes.c_uint, _P]),
     ("fp8gemm_grouped_contiguous", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     ("fp8gemm_grouped_masked", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     ("fp8gemm_dense_small_m_noalloc", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _P]),
@@ -333,10 +334,11 @@ def fp8gemm_dense_ex(A, sA, a_fmt, B, sB, b_fmt, D=None, flags=0, stream=None):
     return D
 
 
-def fp8gemm_dense_quant_a(X, B, sB, D=None, Q=None, sA=None, stream=None):
+def fp8gemm_dense_quant_a(X, B, sB, D=None, Q=None, sA=None, stream=None, flags=0):
     """X f32 [M, K], B u8 [N, K], sB [ceil(N/128), K/128] -> D bf16 [M, N], with A
     quantised 1x128 on load.  Q u8 [M, K] and sA f32 [M, K/128] (both or neither)
-    receive the quantised activations."""
+    receive the quantised activations.  flags (e.g. FLAG_B_READ_ONLY) go to
+    fp8gemm_dense_quant_a_ex."""
     torch = _torch()
     X, B = _f32(X, "X"), _u8(B, "B")
     M, N, K = _dense_mnk(X, B, "X")
@@ -354,9 +356,13 @@ def fp8gemm_dense_quant_a(X, B, sB, D=None, Q=None, sA=None, stream=None):
         _need(_f32(sA, "sA"), "sA", M * Kb, Kb)
     qp = _ptr(_u8(Q, "Q"), "Q") if Q is not None else None
     sp = _ptr(sA, "sA") if sA is not None else None
-    _check(lib().fp8gemm_dense_quant_a(_ptr(X, "X"), qp, sp, _ptr(B, "B"), _ptr(sB, "sB"),
-                                       _ptr(D, "D"), M, N, K, _stream(stream)),
-           "fp8gemm_dense_quant_a")
+    if flags:
+        rc = lib().fp8gemm_dense_quant_a_ex(_ptr(X, "X"), qp, sp, _ptr(B, "B"), _ptr(sB, "sB"),
+                                            _ptr(D, "D"), M, N, K, int(flags), _stream(stream))
+    else:
+        rc = lib().fp8gemm_dense_quant_a(_ptr(X, "X"), qp, sp, _ptr(B, "B"), _ptr(sB, "sB"),
+                                         _ptr(D, "D"), M, N, K, _stream(stream))
+    _check(rc, "fp8gemm_dense_quant_a_ex" if flags else "fp8gemm_dense_quant_a")
     return D
 
 

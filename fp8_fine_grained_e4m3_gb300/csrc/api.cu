@@ -324,10 +324,11 @@ int fp8gemm_dense(const uint8_t* A, const float* sA, const uint8_t* B, const flo
                            stream);
 }
 
-int fp8gemm_dense_quant_a(const float* X, uint8_t* Q, float* sA, const uint8_t* B,
-                          const float* sB, void* D, int M, int N, int K,
-                          fp8gemm_stream_t stream) {
+int fp8gemm_dense_quant_a_ex(const float* X, uint8_t* Q, float* sA, const uint8_t* B,
+                             const float* sB, void* D, int M, int N, int K, unsigned flags,
+                             fp8gemm_stream_t stream) {
   if (int r = check_common(M, N, K)) return r;
+  if (flags & ~unsigned(FP8GEMM_FLAG_B_READ_ONLY)) return FP8GEMM_ERR_FLAGS;
   if (M == 0 || N == 0) return FP8GEMM_OK;
   if (!X || !B || !sB || !D || (Q == nullptr) != (sA == nullptr)) return FP8GEMM_ERR_NULL;
   if (!aligned16(X) || !aligned16(B) || !aligned16(sB) || !aligned16(D) ||
@@ -346,7 +347,14 @@ int fp8gemm_dense_quant_a(const float* X, uint8_t* Q, float* sA, const uint8_t* 
   // the quantiser, then the GEMM as its programmatic dependent: the GEMM's
   // prologue and weight prefetch overlap the quantiser
   if (int r = fp8_quant_1x128(X, Q, sA, M, K, stream)) return r;
-  return fp8gemm_dense(Q, sA, B, sB, D, M, N, K, stream);
+  return fp8gemm_dense_ex(Q, sA, FP8GEMM_FMT_E4M3, B, sB, FP8GEMM_FMT_E4M3, D, M, N, K, flags,
+                          stream);
+}
+
+int fp8gemm_dense_quant_a(const float* X, uint8_t* Q, float* sA, const uint8_t* B,
+                          const float* sB, void* D, int M, int N, int K,
+                          fp8gemm_stream_t stream) {
+  return fp8gemm_dense_quant_a_ex(X, Q, sA, B, sB, D, M, N, K, 0u, stream);
 }
 
 int fp8gemm_grouped_table(const fp8gemm_problem* problems, int num_problems, int max_M,

@@ -210,6 +210,18 @@ int fp8gemm_dense_quant_a(const float* X, uint8_t* Q, float* sA, const uint8_t* 
                           fp8gemm_stream_t stream);
 
 /*
+ * fp8gemm_dense_quant_a_ex -- fp8gemm_dense_quant_a with flags (as
+ * fp8gemm_dense_ex; 0 gives exactly fp8gemm_dense_quant_a).  With
+ * FP8GEMM_FLAG_B_READ_ONLY the decode-path GEMM, launched as the
+ * quantiser's programmatic dependent, stages its first weight tiles while
+ * the quantiser runs -- at decode sizes the quantiser occupies few SMs, so
+ * the GEMM's CTAs find room beside it.
+ */
+int fp8gemm_dense_quant_a_ex(const float* X, uint8_t* Q, float* sA, const uint8_t* B,
+                             const float* sB, void* D, int M, int N, int K, unsigned flags,
+                             fp8gemm_stream_t stream);
+
+/*
  * fp8gemm_grouped_contiguous -- MoE experts in one launch, each expert's
  * tokens a contiguous row segment of A ("news.rkmt.cn/news/5092" section 5.3;
  * "news.rkmt.cn/news/5092" section 1.2: one launch for many experts).

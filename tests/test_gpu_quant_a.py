@@ -90,3 +90,23 @@ def test_quant_a_rejects_half_given_outputs():
     Q = torch.empty((4, 256), dtype=torch.uint8, device="cuda")
     with pytest.raises(ValueError):
         b.fp8gemm_dense_quant_a(X, B, sB, Q=Q)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 7168, 2048), (16, 2048, 7168), (33, 1000, 1280)])
+def test_quant_a_read_only_weights_chain(M, N, K):
+    """fp8gemm_dense_quant_a_ex with FLAG_B_READ_ONLY: the GEMM stages its
+    weights while the quantiser (its predecessor in the stream) runs; the
+    activations come from the kernel just before; three calls back to back."""
+    b = _b()
+    Bq, sB = _weights(N, K, seed=N + 1)
+    tB, tsB = dev(Bq), dev(sB)
+    outs, xs = [], []
+    for seed in (61, 62, 63):
+        X, _ = synthetic.dense_operands(M, 8, K, kind="decode", seed=seed)
+        tX = dev(X * np.float32(0.5)) * 2.0  # written by a kernel just before
+        outs.append(b.fp8gemm_dense_quant_a(tX, tB, tsB, flags=b.FLAG_B_READ_ONLY))
+        xs.append(X)
+    for X, D in zip(xs, outs):
+        Qo, sAo = oquant.quant_1x128_fast(X)
+        assert_close(host(D), ogemm.gemm_dense(Qo, sAo, Bq, sB), "read-only quant-on-load")
+    assert b.fp8gemm_get_device_status() == b.OK
