@@ -63,6 +63,9 @@ struct GemmArgs {
   // running when this one starts writes B or sB: a programmatic dependent may
   // then load weights before waiting for the kernels ahead of it.
   int b_read_only = 0;
+  // Persistent tensor-core GEMM: D's tensor map is valid, so whole 32-row
+  // bands of a tile leave through shared memory and TMA stores.
+  int d_tma = 0;
 };
 
 constexpr int kMaxSplit = 8;  // parts (cluster CTAs) per split tile, at most
@@ -100,5 +103,11 @@ unsigned long long wait_limit_ns();
 // rows x cols bytes, box of box_rows x 128 bytes.  Defined in api.cu.
 bool make_tmap_u8_sw128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                         uint32_t box_rows);
+// Encodes a 2-D row-major bf16 tensor map with 64-byte swizzling: rows x
+// cols elements, box of box_rows x 32 elements (64 bytes).  False when the
+// layout cannot be described (base not 16-byte aligned, cols * 2 not a
+// multiple of 16).  Defined in api.cu.
+bool make_tmap_bf16_sw64(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                         uint32_t box_rows);
 
 }  // namespace fp8gemm

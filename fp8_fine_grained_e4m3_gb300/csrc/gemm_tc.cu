@@ -46,6 +46,8 @@
 // news/5092" section 3.2: size the work to the SM count).  The masked form
 // enumerates only tiles that hold valid rows, so no CTA idles on an empty
 // expert ("lpnh.cn/news/2822121" section 5.2: skip empty blocks).
+#include <cstring>
+
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -79,7 +81,13 @@ struct TcCfg {
   static constexpr int kTmemBufs = 2;       // TMEM partial buffers
   static constexpr int kTmemCols = kTmemBufs * BN;
   static constexpr int kBarBytes = 512;
-  static constexpr size_t kSmemBytes = 1024 + size_t(kStages) * kStageBytes + kBarBytes;
+  // Epilogue staging: two 32-row x 32-column BF16 boxes (2 KB each) per
+  // promotion warp, written alternately while TMA stores drain the other.
+  static constexpr int kEpiBoxBytes = 32 * 32 * 2;
+  static constexpr int kEpiBytes = kPromoWarps * 2 * kEpiBoxBytes;
+  static constexpr size_t kSmemBytes =
+      1024 + size_t(kStages) * kStageBytes + kEpiBytes + kBarBytes;
+  static_assert(kSmemBytes <= 232448, "227 KB of shared memory per CTA");
   static_assert(BN == 128 || BN == 256, "BN");
   static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM columns must be a power of 2");
   static_assert((2 * kStages + 2 * kTmemBufs + 1) * 8 + 8 <= kBarBytes, "barrier area");
@@ -200,7 +208,8 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 template <class Cfg, bool kSplit>
 __global__ void __launch_bounds__(Cfg::kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
-                   const __grid_constant__ CUtensorMap tmB, const GemmArgs args, int* status) {
+                   const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmD, const GemmArgs args, int* status) {
   constexpr int BN = Cfg::BN;
   constexpr int kStages = Cfg::kStages;
 
@@ -209,7 +218,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* smA = smem;
   uint8_t* smB = smem + kStages * Cfg::kABytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * Cfg::kStageBytes);
+  uint8_t* epi = smem + kStages * Cfg::kStageBytes;  // 1024-byte aligned
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi + Cfg::kEpiBytes);
   uint64_t* full_bar = bars;
   uint64_t* empty_bar = bars + kStages;
   uint64_t* tfull_bar = bars + 2 * kStages;
@@ -242,6 +252,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   if (warp == Cfg::kTmaWarp && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (args.d_tma) tma_prefetch_desc(&tmD);
   }
   tc_fence_before();
   __syncthreads();
@@ -351,6 +362,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     const uint32_t lane_base = uint32_t((warp % 4) * 32) << 16;
     const int Nb = ceil_div(args.N, kBlockK);
     uint32_t it = 0;
+    uint32_t n_stores = 0;  // TMA stores this warp has issued (alternates the boxes)
     bool ok = true;
     for (int t = first_tile(t_begin); t < end_tile(t_end) && ok; t += tile_step()) {
       Tile tile;
@@ -419,9 +431,47 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                                  acc[2 * j4 + 1].y);
         continue;
       }
-      // epilogue: BF16 (round to nearest even), 16-byte stores; rows of D
-      // are 16-byte aligned only when N % 8 == 0, else element stores
-      if (row_ok && args.N % 8 != 0) {
+      // epilogue: BF16 (round to nearest even).  A warp whose 32 rows are all
+      // real outputs stages its band 32 columns at a time in one of its two
+      // shared-memory boxes (64-byte swizzle: 16-byte chunk j of row r sits
+      // at chunk j ^ (r / 2 % 4)) and one lane stores each box with TMA:
+      // whole-line writes that drain while the warp goes on.  Other rows
+      // store directly: 16 bytes at a time when rows of D are 16-byte
+      // aligned (N % 8 == 0), else element by element.
+      const int wrow0 = (warp % 4) * 32;  // first tile row of this warp
+      if (args.d_tma && wrow0 + 32 <= tile.valid_rows) {
+        uint8_t* wbox = epi + warp * (2 * Cfg::kEpiBoxBytes);
+#pragma unroll
+        for (int c = 0; c < Cfg::kColsPerWG / 32; ++c) {
+          if (col0 + 32 * c >= args.N) break;  // warp-uniform
+          uint8_t* box = wbox + (n_stores & 1) * Cfg::kEpiBoxBytes;
+          // at most one store pending: the one before it, which used this
+          // box, has finished reading it
+          if (lane == 0) bulk_wait_group_read<1>();
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2* a4 = acc + 16 * c + 4 * j;
+            __nv_bfloat162 p0 = __float22bfloat162_rn(a4[0]);
+            __nv_bfloat162 p1 = __float22bfloat162_rn(a4[1]);
+            __nv_bfloat162 p2 = __float22bfloat162_rn(a4[2]);
+            __nv_bfloat162 p3 = __float22bfloat162_rn(a4[3]);
+            uint4 v;
+            v.x = *reinterpret_cast<uint32_t*>(&p0);
+            v.y = *reinterpret_cast<uint32_t*>(&p1);
+            v.z = *reinterpret_cast<uint32_t*>(&p2);
+            v.w = *reinterpret_cast<uint32_t*>(&p3);
+            *reinterpret_cast<uint4*>(box + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) = v;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmD, box, col0 + 32 * c, tile.row0 + wrow0);
+            bulk_commit_group();
+          }
+          ++n_stores;
+        }
+      } else if (row_ok && args.N % 8 != 0) {
         __nv_bfloat16* drow = args.D + size_t(tile.row0 + row) * args.N + col0;
 #pragma unroll
         for (int j = 0; j < Cfg::kColsPerWG / 2; ++j) {
@@ -448,6 +498,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         }
       }
     }
+    // this warp's TMA stores have completed before its shared memory can go
+    if (lane == 0) bulk_wait_group_all();
   } else {
     regs_decrease<Cfg::kLowRegs>();  // warps 10-11: no work
   }
@@ -569,11 +621,15 @@ template <class Cfg>
 cudaError_t run(const LaunchCtx& c, GemmArgs a, int* launches) {
   *launches = 0;
   a.wait_ns = wait_limit_ns();
-  CUtensorMap tmA, tmB;
+  CUtensorMap tmA, tmB, tmD;
   const uint64_t a_rows = a.mode == GemmMode::kMasked ? uint64_t(a.E) * a.M : uint64_t(a.M);
   const uint64_t b_rows = uint64_t(a.E) * a.N;
   if (!make_tmap_u8_sw128(&tmA, a.A, a_rows, a.K, kBlockM)) return cudaErrorInvalidValue;
   if (!make_tmap_u8_sw128(&tmB, a.B, b_rows, a.K, Cfg::BN)) return cudaErrorInvalidValue;
+  // D has A's row space; without a describable layout (N % 8 != 0, or a base
+  // that is not 16-byte aligned) every row takes the direct stores
+  memset(&tmD, 0, sizeof(tmD));
+  a.d_tma = make_tmap_bf16_sw64(&tmD, a.D, a_rows, uint64_t(a.N), 32) ? 1 : 0;
   if (cudaError_t e = set_smem_attr<Cfg, false>()) return e;
   if (cudaError_t e = set_smem_attr<Cfg, true>()) return e;
 
@@ -588,8 +644,8 @@ cudaError_t run(const LaunchCtx& c, GemmArgs a, int* launches) {
 
   if (a.split == 1) {
     const int grid = int(tiles < c.num_sms ? tiles : c.num_sms);
-    gemm_tc_kernel<Cfg, false><<<grid, Cfg::kThreads, Cfg::kSmemBytes, c.stream>>>(tmA, tmB, a,
-                                                                                c.status);
+    gemm_tc_kernel<Cfg, false><<<grid, Cfg::kThreads, Cfg::kSmemBytes, c.stream>>>(
+        tmA, tmB, tmD, a, c.status);
     if (cudaError_t e = cudaGetLastError()) return e;
   } else {
     // one cluster per tile, as a programmatic dependent (its prologue
@@ -608,7 +664,7 @@ cudaError_t run(const LaunchCtx& c, GemmArgs a, int* launches) {
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    if (cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<Cfg, true>, tmA, tmB, a,
+    if (cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<Cfg, true>, tmA, tmB, tmD, a,
                                            c.status))
       return e;
   }

@@ -120,6 +120,35 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// 2-D tiled store shared -> global of one box (elements outside the tensor
+// are not written), tracked in this thread's bulk async-group; c0 is the
+// innermost coordinate in elements.  The source must have been published to
+// the async proxy (fence_proxy_async_smem by every writing thread, then a
+// barrier) before this thread issues it.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int32_t c0,
+                                             int32_t c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];"
+               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(src)), "r"(c0), "r"(c1)
+               : "memory");
+}
+
+// Closes this thread's pending bulk copies into one bulk async-group.
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Waits until at most N of this thread's bulk async-groups still read their
+// shared-memory source (their global writes may still be in flight).
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// Waits until all of this thread's bulk async-groups have completed.
+__device__ __forceinline__ void bulk_wait_group_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // Same, with an L2 eviction-priority hint (a createpolicy value).
 __device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* map,
                                                  uint64_t* bar, int32_t c0, int32_t c1,
