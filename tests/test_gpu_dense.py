@@ -45,6 +45,11 @@ def _run(A, sA, B, sB):
     (100, 2056, 1040, "prefill"),   # N >= 2048 with a partial 256-wide tile, K % 128 = 16
     (5, 777, 400, "decode"),        # small M: partial K block, N odd
     (48, 3000, 2064, "decode"),     # small M, clusters, partial last K block
+    # a wave or more of whole tiles (CTAs loop over several tiles)
+    (517, 7936, 1024, "prefill"),   # 5 M blocks, the last one 5 rows: TMA and direct stores
+    (1300, 4000, 640, "normal"),    # 11 M blocks, partial last N tile
+    (1300, 1800, 272, "normal"),    # 128-wide N tiles, partial last K block
+    (2100, 2060, 384, "prefill"),   # N % 8 != 0: direct stores only, 17 M blocks
 ])
 def test_dense_matches_oracle(M, N, K, kind):
     A, sA, B, sB = quantised_dense(M, N, K, kind, seed=M * 7 + N)
