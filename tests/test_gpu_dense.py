@@ -50,6 +50,9 @@ def _run(A, sA, B, sB):
     (1300, 4000, 640, "normal"),    # 11 M blocks, partial last N tile
     (1300, 1800, 272, "normal"),    # 128-wide N tiles, partial last K block
     (2100, 2060, 384, "prefill"),   # N % 8 != 0: direct stores only, 17 M blocks
+    # deeper K with a partial last round of tiles
+    (2100, 2060, 2048, "prefill"),  # 153 tiles: one CTA takes a second tile
+    (1700, 4096, 2560, "normal"),   # 224 tiles: 72 CTAs take a second tile
 ])
 def test_dense_matches_oracle(M, N, K, kind):
     A, sA, B, sB = quantised_dense(M, N, K, kind, seed=M * 7 + N)

@@ -38,7 +38,8 @@ def test_contiguous_two_experts_eight_tokens():
 
 
 @pytest.mark.parametrize("E,T,N,K", [(5, 300, 384, 512), (8, 1000, 512, 1024), (3, 200, 2048, 256),
-                                     (4, 300, 300, 400)])  # partial last K block, N % 8 != 0
+                                     (4, 300, 300, 400),  # partial last K block, N % 8 != 0
+                                     (6, 2500, 4096, 2048)])  # 368 tiles: a partial last round
 def test_contiguous_matches_oracle(E, T, N, K):
     A, sA, B, sB, lay = _contig_case(E, T, N, K, seed=E + T)
     got = _run_contig(A, sA, B, sB, lay.m_indices)
@@ -109,6 +110,8 @@ def _run_masked(A, sA, B, sB, mm):
     (3, 256, 512, 512, [256, 1, 128]),
     (6, 64, 2048, 384, [64, 0, 0, 63, 1, 17]),
     (3, 200, 250, 272, [200, 7, 0]),  # partial last K block, N % 8 != 0
+    # 160 tiles over the SMs: 8 CTAs take a second tile
+    (10, 128, 4096, 4096, [128, 1, 77, 128, 5, 100, 128, 64, 3, 128]),
 ])
 def test_masked_matches_oracle_and_leaves_rows(E, M_max, N, K, mm):
     mm = np.array(mm, np.int32)
