@@ -43,6 +43,8 @@ SIGNATURES = [
     ("fp8gemm_dense", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _P]),
     ("fp8_quant_1x128_fmt", _I, [_P, _P, _P, _I, _I, _I, _P]),
     ("fp8_quant_128x128_fmt", _I, [_P, _P, _P, _I, _I, _I, _I, _P]),
+    ("fp8_quant_1x128_ex", _I, [_P, _P, _P, _I, _I, _I, _P, _P]),
+    ("fp8_quant_128x128_ex", _I, [_P, _P, _P, _I, _I, _I, _I, _P, _P]),
     ("fp8gemm_dense_fmt", _I, [_P, _P, _I, _P, _P, _I, _P, _I, _I, _I, _P]),
     ("fp8gemm_dense_ex", _I, [_P, _P, _I, _P, _P, _I, _P, _I, _I, _I, ctypes.c_uint, _P]),
     ("fp8gemm_grouped_table", _I, [_P, _I, _I, _P]),
@@ -270,8 +272,21 @@ def _u8_fmt(t, fmt, name):
     return t
 
 
-def fp8_quant_1x128_fmt(X, fmt, Q=None, sX=None, stream=None):
-    """fp8_quant_1x128 with the output format ("e4m3" or "e5m2")."""
+def _counter(t):
+    """Device address of a saturation counter: an int64 CUDA tensor (its
+    first element is added to), or None."""
+    torch = _torch()
+    if t is None:
+        return None
+    if t.dtype != torch.int64 or t.numel() < 1:
+        raise TypeError(f"sat_count must be an int64 tensor of at least one element, got {t.dtype}")
+    return _ptr(t, "sat_count")
+
+
+def fp8_quant_1x128_fmt(X, fmt, Q=None, sX=None, stream=None, sat_count=None):
+    """fp8_quant_1x128 with the output format ("e4m3" or "e5m2").  sat_count
+    (an int64 CUDA tensor) receives, added to its first element, the number of
+    values the saturating encoding clamped (fp8_quant_1x128_ex)."""
     torch = _torch()
     X = _f32(X, "X")
     K = X.shape[-1]
@@ -282,13 +297,19 @@ def fp8_quant_1x128_fmt(X, fmt, Q=None, sX=None, stream=None):
         sX = torch.empty((*X.shape[:-1], _cdiv(K, 128)), dtype=torch.float32, device=X.device)
     Q = _need(_u8_fmt(Q, fmt, "Q"), "Q", M * K, K)
     _need(_f32(sX, "sX"), "sX", M * _cdiv(K, 128), _cdiv(K, 128))
+    if sat_count is not None:
+        _check(lib().fp8_quant_1x128_ex(_ptr(X, "X"), _ptr(Q, "Q"), _ptr(sX, "sX"), M, K,
+                                        _fmt(fmt), _counter(sat_count), _stream(stream)),
+               "fp8_quant_1x128_ex")
+        return Q, sX
     _check(lib().fp8_quant_1x128_fmt(_ptr(X, "X"), _ptr(Q, "Q"), _ptr(sX, "sX"), M, K, _fmt(fmt),
                                      _stream(stream)), "fp8_quant_1x128_fmt")
     return Q, sX
 
 
-def fp8_quant_128x128_fmt(W, fmt, Q=None, sW=None, stream=None):
-    """fp8_quant_128x128 with the output format ("e4m3" or "e5m2")."""
+def fp8_quant_128x128_fmt(W, fmt, Q=None, sW=None, stream=None, sat_count=None):
+    """fp8_quant_128x128 with the output format ("e4m3" or "e5m2"); sat_count
+    as for fp8_quant_1x128_fmt (fp8_quant_128x128_ex)."""
     torch = _torch()
     W, squeeze, W3 = _weights3(W)
     E, N, K = W3.shape
@@ -299,6 +320,11 @@ def fp8_quant_128x128_fmt(W, fmt, Q=None, sW=None, stream=None):
         sW = torch.empty(shp if squeeze else (E, *shp), dtype=torch.float32, device=W.device)
     Qb = _need(_u8_fmt(Q, fmt, "Q"), "Q", E * N * K, K)
     _need(_f32(sW, "sW"), "sW", E * shp[0] * shp[1], shp[1])
+    if sat_count is not None:
+        _check(lib().fp8_quant_128x128_ex(_ptr(W3, "W"), _ptr(Qb, "Q"), _ptr(sW, "sW"), E, N, K,
+                                          _fmt(fmt), _counter(sat_count), _stream(stream)),
+               "fp8_quant_128x128_ex")
+        return Q, sW
     _check(lib().fp8_quant_128x128_fmt(_ptr(W3, "W"), _ptr(Qb, "Q"), _ptr(sW, "sW"), E, N, K,
                                        _fmt(fmt), _stream(stream)), "fp8_quant_128x128_fmt")
     return Q, sW

@@ -262,16 +262,22 @@ void count_kernel_launches(int n) { g_launches += n; }
 
 extern "C" {
 
-int fp8_quant_1x128_fmt(const float* X, uint8_t* Q, float* sX, int M, int K, int fmt,
-                        fp8gemm_stream_t stream) {
+int fp8_quant_1x128_ex(const float* X, uint8_t* Q, float* sX, int M, int K, int fmt,
+                       unsigned long long* sat_count, fp8gemm_stream_t stream) {
   if (M < 0 || K < 0 || K % kKAlign != 0) return FP8GEMM_ERR_SHAPE;
   if (fmt != FP8GEMM_FMT_E4M3 && fmt != FP8GEMM_FMT_E5M2) return FP8GEMM_ERR_FORMAT;
   if (M == 0 || K == 0) return FP8GEMM_OK;
   if (!X || !Q || !sX) return FP8GEMM_ERR_NULL;
   if (!aligned16(X) || !aligned16(Q) || !aligned16(sX)) return FP8GEMM_ERR_ALIGN;
+  if (reinterpret_cast<uintptr_t>(sat_count) % 8 != 0) return FP8GEMM_ERR_ALIGN;
   LaunchCtx c;
   if (int r = ctx_for(stream, &c)) return r;
-  return finish(launch_quant_1x128(c, X, Q, sX, M, K, fmt), 1);
+  return finish(launch_quant_1x128(c, X, Q, sX, M, K, fmt, sat_count), 1);
+}
+
+int fp8_quant_1x128_fmt(const float* X, uint8_t* Q, float* sX, int M, int K, int fmt,
+                        fp8gemm_stream_t stream) {
+  return fp8_quant_1x128_ex(X, Q, sX, M, K, fmt, nullptr, stream);
 }
 
 int fp8_quant_1x128(const float* X, uint8_t* Q, float* sX, int M, int K,
@@ -279,17 +285,23 @@ int fp8_quant_1x128(const float* X, uint8_t* Q, float* sX, int M, int K,
   return fp8_quant_1x128_fmt(X, Q, sX, M, K, FP8GEMM_FMT_E4M3, stream);
 }
 
-int fp8_quant_128x128_fmt(const float* W, uint8_t* Q, float* sW, int E, int N, int K, int fmt,
-                          fp8gemm_stream_t stream) {
+int fp8_quant_128x128_ex(const float* W, uint8_t* Q, float* sW, int E, int N, int K, int fmt,
+                         unsigned long long* sat_count, fp8gemm_stream_t stream) {
   if (E < 0 || N < 0 || K < 0 || K % kKAlign != 0) return FP8GEMM_ERR_SHAPE;
   if (fmt != FP8GEMM_FMT_E4M3 && fmt != FP8GEMM_FMT_E5M2) return FP8GEMM_ERR_FORMAT;
   if (E == 0 || N == 0 || K == 0) return FP8GEMM_OK;
   if ((long long)E * N * (long long)K > (1LL << 46)) return FP8GEMM_ERR_SHAPE;
   if (!W || !Q || !sW) return FP8GEMM_ERR_NULL;
   if (!aligned16(W) || !aligned16(Q) || !aligned16(sW)) return FP8GEMM_ERR_ALIGN;
+  if (reinterpret_cast<uintptr_t>(sat_count) % 8 != 0) return FP8GEMM_ERR_ALIGN;
   LaunchCtx c;
   if (int r = ctx_for(stream, &c)) return r;
-  return finish(launch_quant_128x128(c, W, Q, sW, E, N, K, fmt), 1);
+  return finish(launch_quant_128x128(c, W, Q, sW, E, N, K, fmt, sat_count), 1);
+}
+
+int fp8_quant_128x128_fmt(const float* W, uint8_t* Q, float* sW, int E, int N, int K, int fmt,
+                          fp8gemm_stream_t stream) {
+  return fp8_quant_128x128_ex(W, Q, sW, E, N, K, fmt, nullptr, stream);
 }
 
 int fp8_quant_128x128(const float* W, uint8_t* Q, float* sW, int E, int N, int K,

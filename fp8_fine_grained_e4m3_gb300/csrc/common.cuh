@@ -32,10 +32,13 @@ struct LaunchCtx {
   int* status;  // device address of the status word
 };
 
+// The quantisers; sat (device, may be null) receives the saturation count.
 cudaError_t launch_quant_1x128(const LaunchCtx& c, const float* X, uint8_t* Q, float* sX,
-                               int M, int K, int fmt = FP8GEMM_FMT_E4M3);
+                               int M, int K, int fmt = FP8GEMM_FMT_E4M3,
+                               unsigned long long* sat = nullptr);
 cudaError_t launch_quant_128x128(const LaunchCtx& c, const float* W, uint8_t* Q, float* sW,
-                                 int E, int N, int K, int fmt = FP8GEMM_FMT_E4M3);
+                                 int E, int N, int K, int fmt = FP8GEMM_FMT_E4M3,
+                                 unsigned long long* sat = nullptr);
 
 // Problem description for the persistent tensor-core GEMM.
 enum class GemmMode : int { kDense = 0, kContiguous = 1, kMasked = 2 };

@@ -11,6 +11,16 @@
 // Both kernels are bandwidth-bound (4 bytes read, 1 + 4/128 bytes written
 // per element): loads are 16-byte vectors and every warp writes whole 128-byte
 // output rows.
+//
+// Optional saturation count ("blog.hotdry.top: DeepGEMM FP8 GEMM
+// fine-grained scaling kernels", section on numerical-stability checks and
+// monitoring: track how many FP8 conversions overflow): the number of
+// elements of blocks with amax != 0 whose FP32 quotient x / s is not within
+// +-limit -- exactly the values the saturating conversion clamps (or, for a
+// quotient that is NaN, cannot represent).  With the per-block scale that only
+// happens when rounding pushes x / s just past the limit, or when amax / limit
+// underflows to 0.  Counted per lane, summed per warp (or CTA) and added once
+// to the caller's 64-bit counter, and only in the instances that count.
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -30,17 +40,24 @@ __device__ __forceinline__ uint32_t cvt_f8x2(float lo, float hi) {
   return r;
 }
 
-template <bool kE5M2>
-__device__ __forceinline__ uint32_t quant4(float4 v, float s) {
-  const float q0 = __fdiv_rn(v.x, s), q1 = __fdiv_rn(v.y, s);
-  const float q2 = __fdiv_rn(v.z, s), q3 = __fdiv_rn(v.w, s);
-  return cvt_f8x2<kE5M2>(q0, q1) | (cvt_f8x2<kE5M2>(q2, q3) << 16);
-}
-
 // The format's largest finite value: the divisor of the scale rule.
 template <bool kE5M2>
 __device__ __forceinline__ float f8_limit() {
   return kE5M2 ? 57344.0f : kE4M3Max;
+}
+
+// Four values -> four FP8 bytes (x / s each); kCount: adds to n the
+// quotients the conversion clamps (not within +-limit, NaN included).
+template <bool kE5M2, bool kCount = false>
+__device__ __forceinline__ uint32_t quant4(float4 v, float s, unsigned* n = nullptr) {
+  const float q0 = __fdiv_rn(v.x, s), q1 = __fdiv_rn(v.y, s);
+  const float q2 = __fdiv_rn(v.z, s), q3 = __fdiv_rn(v.w, s);
+  if constexpr (kCount) {
+    const float lim = f8_limit<kE5M2>();
+    *n += unsigned(!(fabsf(q0) <= lim)) + unsigned(!(fabsf(q1) <= lim)) +
+          unsigned(!(fabsf(q2) <= lim)) + unsigned(!(fabsf(q3) <= lim));
+  }
+  return cvt_f8x2<kE5M2>(q0, q1) | (cvt_f8x2<kE5M2>(q2, q3) << 16);
 }
 
 __device__ __forceinline__ float absmax4(float4 v) {
@@ -56,11 +73,13 @@ constexpr int kQuantUnroll = 4;  // 1x128 blocks per warp (loads kept in flight)
 // K % 128 remaining elements (a multiple of 16) and its amax runs over those.
 // kPdl: launched as a programmatic dependent of the previous kernel (wait for
 // it before the first load; let the next kernel launch right away).
-template <bool kPdl, bool kRagged, bool kE5M2>
+// kCount: add the saturation count to *sat.
+template <bool kPdl, bool kRagged, bool kE5M2, bool kCount>
 __global__ void __launch_bounds__(256) quant_1x128_kernel(const float* __restrict__ X,
                                                           uint32_t* __restrict__ Q,
                                                           float* __restrict__ sX,
-                                                          long long nblocks, int K, int Kb) {
+                                                          long long nblocks, int K, int Kb,
+                                                          unsigned long long* sat) {
   const long long warp0 =
       ((long long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32) * kQuantUnroll;
   const int lane = threadIdx.x % 32;
@@ -86,6 +105,7 @@ __global__ void __launch_bounds__(256) quant_1x128_kernel(const float* __restric
     v[u] = in[u] ? __ldcs(reinterpret_cast<const float4*>(X + e0[u]) + lane)
                  : make_float4(0.f, 0.f, 0.f, 0.f);
   }
+  unsigned n_sat = 0;
 #pragma unroll
   for (int u = 0; u < kQuantUnroll; ++u) {
     const long long b = warp0 + u;
@@ -94,19 +114,24 @@ __global__ void __launch_bounds__(256) quant_1x128_kernel(const float* __restric
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     const float s = __fdiv_rn(amax, f8_limit<kE5M2>());
-    if (in[u]) Q[e0[u] / 4 + lane] = amax != 0.f ? quant4<kE5M2>(v[u], s) : 0u;
+    if (in[u]) Q[e0[u] / 4 + lane] = amax != 0.f ? quant4<kE5M2, kCount>(v[u], s, &n_sat) : 0u;
     if (lane == 0) sX[b] = s;
+  }
+  if constexpr (kCount) {
+    n_sat = __reduce_add_sync(0xffffffffu, n_sat);
+    if (lane == 0 && n_sat != 0) atomicAdd(sat, (unsigned long long)n_sat);
   }
 }
 
 // One CTA (256 threads) per 128x128 tile of one [N, K] matrix of the batch.
 // Thread t covers column group t % 32 (4 columns) of rows t / 32 + 8 i.
 // The last K tile may be partial (K % 128 columns, a multiple of 16).
-template <bool kE5M2>
+// kCount: add the saturation count to *sat.
+template <bool kE5M2, bool kCount>
 __global__ void __launch_bounds__(256) quant_128x128_kernel(const float* __restrict__ W,
                                                             uint8_t* __restrict__ Q,
                                                             float* __restrict__ sW, int N,
-                                                            int K) {
+                                                            int K, unsigned long long* sat) {
   const int Kb = ceil_div(K, kBlockK);
   const int Nb = ceil_div(N, 128);
   const int kb = blockIdx.x;
@@ -138,24 +163,38 @@ __global__ void __launch_bounds__(256) quant_128x128_kernel(const float* __restr
 #pragma unroll
   for (int w = 1; w < 8; ++w) amax = fmaxf(amax, red[w]);
   const float s = __fdiv_rn(amax, f8_limit<kE5M2>());
+  unsigned n_sat = 0;
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const int n = nb * 128 + r0 + 8 * i;
     if (n < N && col_in) {
       uint32_t* dst = reinterpret_cast<uint32_t*>(Q + mat + size_t(n) * K + kb * kBlockK) + cg;
-      *dst = amax != 0.f ? quant4<kE5M2>(v[i], s) : 0u;
+      *dst = amax != 0.f ? quant4<kE5M2, kCount>(v[i], s, &n_sat) : 0u;
     }
   }
   if (threadIdx.x == 0) sW[(size_t(e) * Nb + nb) * Kb + kb] = s;
+  if constexpr (kCount) {
+    // amax (and so every thread's path above) is uniform over the CTA
+    __shared__ unsigned cnt[8];
+    n_sat = __reduce_add_sync(0xffffffffu, n_sat);
+    if (cg == 0) cnt[r0] = n_sat;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      unsigned t = 0;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) t += cnt[w];
+      if (t != 0) atomicAdd(sat, (unsigned long long)t);
+    }
+  }
 }
 
 }  // namespace
 
 namespace {
 
-template <bool kE5M2>
+template <bool kE5M2, bool kCount>
 cudaError_t launch_1x128(const LaunchCtx& c, const float* X, uint8_t* Q, float* sX, int M,
-                         int K) {
+                         int K, unsigned long long* sat) {
   const int Kb = ceil_div(K, kBlockK);
   const long long nblocks = (long long)M * Kb;
   if (nblocks == 0) return cudaSuccess;
@@ -166,11 +205,11 @@ cudaError_t launch_1x128(const LaunchCtx& c, const float* X, uint8_t* Q, float* 
   uint32_t* Q4 = reinterpret_cast<uint32_t*>(Q);
   if (grid > 8LL * c.num_sms) {  // more than one wave: plain launch
     if (ragged)
-      quant_1x128_kernel<false, true, kE5M2>
-          <<<unsigned(grid), 256, 0, c.stream>>>(X, Q4, sX, nblocks, K, Kb);
+      quant_1x128_kernel<false, true, kE5M2, kCount>
+          <<<unsigned(grid), 256, 0, c.stream>>>(X, Q4, sX, nblocks, K, Kb, sat);
     else
-      quant_1x128_kernel<false, false, kE5M2>
-          <<<unsigned(grid), 256, 0, c.stream>>>(X, Q4, sX, nblocks, K, Kb);
+      quant_1x128_kernel<false, false, kE5M2, kCount>
+          <<<unsigned(grid), 256, 0, c.stream>>>(X, Q4, sX, nblocks, K, Kb, sat);
     return cudaGetLastError();
   }
   // A decode-sized quantisation (one wave) is launched as a programmatic
@@ -187,30 +226,40 @@ cudaError_t launch_1x128(const LaunchCtx& c, const float* X, uint8_t* Q, float* 
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   if (ragged)
-    return cudaLaunchKernelEx(&cfg, quant_1x128_kernel<true, true, kE5M2>, X, Q4, sX, nblocks,
-                              K, Kb);
-  return cudaLaunchKernelEx(&cfg, quant_1x128_kernel<true, false, kE5M2>, X, Q4, sX, nblocks,
-                            K, Kb);
+    return cudaLaunchKernelEx(&cfg, quant_1x128_kernel<true, true, kE5M2, kCount>, X, Q4, sX,
+                              nblocks, K, Kb, sat);
+  return cudaLaunchKernelEx(&cfg, quant_1x128_kernel<true, false, kE5M2, kCount>, X, Q4, sX,
+                            nblocks, K, Kb, sat);
 }
 
 }  // namespace
 
 cudaError_t launch_quant_1x128(const LaunchCtx& c, const float* X, uint8_t* Q, float* sX,
-                               int M, int K, int fmt) {
-  return fmt == FP8GEMM_FMT_E5M2 ? launch_1x128<true>(c, X, Q, sX, M, K)
-                                 : launch_1x128<false>(c, X, Q, sX, M, K);
+                               int M, int K, int fmt, unsigned long long* sat) {
+  if (sat != nullptr)
+    return fmt == FP8GEMM_FMT_E5M2 ? launch_1x128<true, true>(c, X, Q, sX, M, K, sat)
+                                   : launch_1x128<false, true>(c, X, Q, sX, M, K, sat);
+  return fmt == FP8GEMM_FMT_E5M2 ? launch_1x128<true, false>(c, X, Q, sX, M, K, nullptr)
+                                 : launch_1x128<false, false>(c, X, Q, sX, M, K, nullptr);
 }
 
 cudaError_t launch_quant_128x128(const LaunchCtx& c, const float* W, uint8_t* Q, float* sW,
-                                 int E, int N, int K, int fmt) {
+                                 int E, int N, int K, int fmt, unsigned long long* sat) {
   if (E == 0 || N == 0 || K == 0) return cudaSuccess;
   const int Nb = ceil_div(N, 128);
   if (Nb > 65535 || E > 65535) return cudaErrorInvalidValue;
   dim3 grid(ceil_div(K, kBlockK), Nb, E);
-  if (fmt == FP8GEMM_FMT_E5M2)
-    quant_128x128_kernel<true><<<grid, 256, 0, c.stream>>>(W, Q, sW, N, K);
-  else
-    quant_128x128_kernel<false><<<grid, 256, 0, c.stream>>>(W, Q, sW, N, K);
+  const bool e5 = fmt == FP8GEMM_FMT_E5M2;
+  if (sat != nullptr) {
+    if (e5)
+      quant_128x128_kernel<true, true><<<grid, 256, 0, c.stream>>>(W, Q, sW, N, K, sat);
+    else
+      quant_128x128_kernel<false, true><<<grid, 256, 0, c.stream>>>(W, Q, sW, N, K, sat);
+  } else if (e5) {
+    quant_128x128_kernel<true, false><<<grid, 256, 0, c.stream>>>(W, Q, sW, N, K, nullptr);
+  } else {
+    quant_128x128_kernel<false, false><<<grid, 256, 0, c.stream>>>(W, Q, sW, N, K, nullptr);
+  }
   return cudaGetLastError();
 }
 

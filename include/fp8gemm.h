@@ -137,6 +137,33 @@ int fp8_quant_128x128_fmt(const float* W, uint8_t* Q, float* sW, int E, int N, i
                           fp8gemm_stream_t stream);
 
 /*
+ * fp8_quant_1x128_ex / fp8_quant_128x128_ex -- the _fmt calls with an
+ * optional saturation counter, for monitoring FP8 overflow in production
+ * ("blog.hotdry.top: DeepGEMM FP8 GEMM fine-grained scaling kernels",
+ * section on numerical-stability checks and monitoring, which lists an FP8
+ * overflow count among the metrics to watch).
+ *
+ *   sat_count  device address of a 64-bit counter (8-byte aligned), or NULL.
+ *              The call ADDS to it (it is never reset here: zero it once and
+ *              it accumulates over calls) the number of elements x of blocks
+ *              with amax != 0 whose FP32 quotient x / s is not within
+ *              +-limit (448 e4m3, 57344 e5m2) -- the values the saturating
+ *              encoding clamps.  With s = amax / limit this happens only when
+ *              FP32 rounding pushes x / s just past the limit (one element of
+ *              a few percent of Gaussian blocks) or when amax / limit
+ *              underflows to 0 (|amax| < about 6e-43 for e4m3; every element
+ *              of such a block then counts).  Finite inputs only.
+ *   NULL: the bytes, scales and launch of the _fmt call; with a counter the
+ *   bytes and scales are the same.  A misaligned counter: FP8GEMM_ERR_ALIGN.
+ *   Asynchronous on `stream` like the rest: read the counter after the
+ *   stream has reached this call.
+ */
+int fp8_quant_1x128_ex(const float* X, uint8_t* Q, float* sX, int M, int K, int fmt,
+                       unsigned long long* sat_count, fp8gemm_stream_t stream);
+int fp8_quant_128x128_ex(const float* W, uint8_t* Q, float* sW, int E, int N, int K, int fmt,
+                         unsigned long long* sat_count, fp8gemm_stream_t stream);
+
+/*
  * fp8gemm_dense -- D = A * B^T with block scales ("lpnh.cn/news/2822121"
  * section 4.1 dense main loop; scaling as above).
  *

@@ -148,6 +148,53 @@ def quant_128x128_grouped(W: np.ndarray):
     return np.stack(qs), np.stack(ss)
 
 
+def _block_saturations(x: np.ndarray, fmt: str = "e4m3") -> int:
+    """Saturations of one block: the steps of :func:`_quant_block` up to the
+    quotient, then the number of elements whose FP32 quotient x / s is not
+    within +-limit (a NaN quotient included) -- the values the saturating
+    encoding clamps.  A block with amax = 0 forms no quotient and counts 0.
+
+    Monitoring an FP8 overflow count: "blog.hotdry.top: DeepGEMM FP8 GEMM
+    fine-grained scaling kernels", section on numerical-stability checks and
+    monitoring."""
+    limit, _ = _FORMATS[fmt]
+    x = np.asarray(x, dtype=np.float32)
+    amax = np.float32(np.max(np.abs(x))) if x.size else np.float32(0.0)
+    if amax == 0:
+        return 0
+    s = np.float32(amax / np.float32(limit))
+    with np.errstate(divide="ignore", invalid="ignore"):
+        y = (x / s).astype(np.float32)  # IEEE FP32 division, round to nearest
+    return int(np.count_nonzero(~(np.abs(y) <= np.float32(limit))))
+
+
+def saturations_1x128(X: np.ndarray, fmt: str = "e4m3") -> int:
+    """Total saturations of :func:`quant_1x128` on X f32 [M, K]: the sum of
+    :func:`_block_saturations` over its (row, K block) blocks."""
+    X = np.ascontiguousarray(X, dtype=np.float32)
+    M, K = X.shape
+    n = 0
+    for m in range(M):
+        for kb in range(-(-K // BLOCK)):
+            n += _block_saturations(X[m, kb * BLOCK:min(K, (kb + 1) * BLOCK)], fmt)
+    return n
+
+
+def saturations_128x128(W: np.ndarray, fmt: str = "e4m3") -> int:
+    """Total saturations of :func:`quant_128x128` on W f32 [N, K] (or a batch
+    [E, N, K]): the sum over its 128x128 tiles."""
+    W = np.asarray(W, dtype=np.float32)
+    if W.ndim == 3:
+        return sum(saturations_128x128(w, fmt) for w in W)
+    N, K = W.shape
+    n = 0
+    for nb in range(-(-N // BLOCK)):
+        for kb in range(-(-K // BLOCK)):
+            n += _block_saturations(W[nb * BLOCK:min(N, (nb + 1) * BLOCK),
+                                      kb * BLOCK:min(K, (kb + 1) * BLOCK)], fmt)
+    return n
+
+
 def dequant_1x128(Q: np.ndarray, S: np.ndarray, fmt: str = "e4m3") -> np.ndarray:
     """dec(q) * s per element (float64), for error-bound checks."""
     decode = e4m3.decode if fmt == "e4m3" else e5m2.decode

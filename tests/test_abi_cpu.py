@@ -98,6 +98,14 @@ def test_host_validation_needs_no_gpu(lib):
     assert lib.fp8gemm_dense_ex(good, good, 0, good, good, 0, good, 4, 256, 136, 1, s) == b.ERR_SHAPE
     assert lib.fp8gemm_dense_ex(good, good, 0, good, good, 0, good, 0, 256, 256, 1, s) == b.OK
     assert b.strerror(b.ERR_FLAGS).startswith("unknown flag")
+    # saturation counters: optional, 8-byte aligned; validated before any CUDA call
+    assert lib.fp8_quant_1x128_ex(good, good, good, 4, 256, 0, P((1 << 20) + 4), s) == b.ERR_ALIGN
+    assert lib.fp8_quant_1x128_ex(good, good, good, 4, 130, 0, good, s) == b.ERR_SHAPE
+    assert lib.fp8_quant_1x128_ex(good, good, good, 4, 256, 3, None, s) == b.ERR_FORMAT
+    assert lib.fp8_quant_1x128_ex(good, good, good, 0, 256, 0, good, s) == b.OK
+    assert lib.fp8_quant_128x128_ex(good, good, good, 1, 8, 128, 0, P((1 << 20) + 12), s) == b.ERR_ALIGN
+    assert lib.fp8_quant_128x128_ex(good, None, good, 1, 8, 128, 0, good, s) == b.ERR_NULL
+    assert lib.fp8_quant_128x128_ex(good, good, good, 1, 0, 128, 1, good, s) == b.OK
 
 
 def test_problem_struct_layout():

@@ -85,3 +85,45 @@ def test_quant_zero_rows_is_noop():
     X = torch.zeros((0, 256), dtype=torch.float32, device="cuda")
     Q, S = _binding().fp8_quant_1x128(X)
     assert Q.shape == (0, 256) and S.shape == (0, 2)
+
+
+@pytest.mark.parametrize("M,K,fmt,kind", [(300, 1024, "e4m3", "normal"), (257, 4096, "e4m3", "prefill"),
+                                          (130, 400, "e4m3", "normal"),   # ragged last K block
+                                          (200, 768, "e5m2", "normal"), (3000, 400, "e4m3", "prefill"),
+                                          (16, 7168, "e4m3", "decode")])  # one wave: the PDL launch
+def test_quant_1x128_saturation_count(M, K, fmt, kind):
+    """fp8_quant_1x128_ex: the count equals the oracle's, the bytes and scales
+    are those of the call without a counter, and the counter accumulates."""
+    import torch
+    b = _binding()
+    X, _ = synthetic.dense_operands(M, 8, K, kind=kind, seed=M * 3 + K)
+    X[min(7, M - 1), :128] = np.float32(1e-44) * (np.arange(128) % 2)  # amax / limit underflows
+    want = oquant.saturations_1x128(X, fmt)
+    assert want > 0
+    cnt = torch.zeros(1, dtype=torch.int64, device="cuda")
+    Q, S = b.fp8_quant_1x128_fmt(dev(X), fmt, sat_count=cnt)
+    Q0, S0 = b.fp8_quant_1x128_fmt(dev(X), fmt)
+    assert int(cnt.item()) == want
+    assert np.array_equal(host(Q), host(Q0))
+    assert np.array_equal(host(S).view(np.uint32), host(S0).view(np.uint32))
+    b.fp8_quant_1x128_fmt(dev(X), fmt, sat_count=cnt)
+    assert int(cnt.item()) == 2 * want
+
+
+@pytest.mark.parametrize("E,N,K,fmt", [(1, 300, 640, "e4m3"), (3, 256, 400, "e4m3"),
+                                       (2, 200, 256, "e5m2")])
+def test_quant_128x128_saturation_count(E, N, K, fmt):
+    import torch
+    b = _binding()
+    g = np.random.default_rng(E * 100 + N)
+    W = g.standard_normal((E, N, K)).astype(np.float32)
+    W[0, :128, :128] = 0
+    W[0, 5, 3] = np.float32(1e-44)  # one tile whose scale underflows
+    want = oquant.saturations_128x128(W, fmt)
+    assert want > 0
+    cnt = torch.zeros(1, dtype=torch.int64, device="cuda")
+    Q, S = b.fp8_quant_128x128_fmt(dev(W), fmt, sat_count=cnt)
+    Q0, S0 = b.fp8_quant_128x128_fmt(dev(W), fmt)
+    assert int(cnt.item()) == want
+    assert np.array_equal(host(Q), host(Q0))
+    assert np.array_equal(host(S).view(np.uint32), host(S0).view(np.uint32))

@@ -107,3 +107,59 @@ def test_gemm_mutants_are_caught(monkeypatch):
                   or _fails(T_gemm.test_dequantise_then_matmul))
         assert caught, mutant.__name__
         monkeypatch.undo()
+
+
+def test_saturation_count_mutants_are_caught(monkeypatch):
+    from tests import test_oracle_saturation as T_sat
+    limit = np.float32(448)
+
+    def counts_equal(x, fmt="e4m3"):
+        # quotients equal to the limit counted too
+        x = np.asarray(x, dtype=np.float32)
+        amax = np.float32(np.max(np.abs(x)))
+        if amax == 0:
+            return 0
+        s = np.float32(amax / limit)
+        with np.errstate(divide="ignore", invalid="ignore"):
+            y = (x / s).astype(np.float32)
+        return int(np.count_nonzero(~(np.abs(y) < limit)))
+
+    def recip(x, fmt="e4m3"):
+        # reciprocal-multiply instead of the division
+        x = np.asarray(x, dtype=np.float32)
+        amax = np.float32(np.max(np.abs(x)))
+        if amax == 0:
+            return 0
+        s = np.float32(amax / limit)
+        with np.errstate(divide="ignore", invalid="ignore"):
+            y = (x * np.float32(np.float32(1) / s)).astype(np.float32)
+        return int(np.count_nonzero(~(np.abs(y) <= limit)))
+
+    def wide_scale(x, fmt="e4m3"):
+        # the scale kept in double: no FP32 rounding of amax / 448
+        x = np.asarray(x, dtype=np.float32)
+        amax = float(np.max(np.abs(x)))
+        if amax == 0:
+            return 0
+        with np.errstate(divide="ignore", invalid="ignore"):
+            y = (x.astype(np.float64) / (amax / 448.0))
+        return int(np.count_nonzero(~(np.abs(y) <= 448.0)))
+
+    def nan_not_counted(x, fmt="e4m3"):
+        x = np.asarray(x, dtype=np.float32)
+        amax = np.float32(np.max(np.abs(x)))
+        if amax == 0:
+            return 0
+        s = np.float32(amax / limit)
+        with np.errstate(divide="ignore", invalid="ignore"):
+            y = (x / s).astype(np.float32)
+        return int(np.count_nonzero(np.abs(y) > limit))
+
+    pins = (T_sat.test_amax_element_against_exact_rounding,
+            T_sat.test_quotient_equal_to_limit_is_not_counted,
+            T_sat.test_zero_block_and_underflowing_scale,
+            T_sat.test_power_of_two_scales_never_saturate)
+    for mutant in (counts_equal, recip, wide_scale, nan_not_counted):
+        monkeypatch.setattr(quant, "_block_saturations", mutant)
+        assert any(_fails(p) for p in pins), mutant.__name__
+        monkeypatch.undo()
