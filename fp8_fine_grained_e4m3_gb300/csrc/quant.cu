@@ -123,12 +123,17 @@ __global__ void __launch_bounds__(256) quant_1x128_kernel(const float* __restric
   }
 }
 
-// One CTA (256 threads) per 128x128 tile of one [N, K] matrix of the batch.
-// Thread t covers column group t % 32 (4 columns) of rows t / 32 + 8 i.
-// The last K tile may be partial (K % 128 columns, a multiple of 16).
-// kCount: add the saturation count to *sat.
+// One CTA (kQ2Threads threads) per 128x128 tile of one [N, K] matrix of the
+// batch.  Thread t covers column group t % 32 (4 columns) of rows
+// t / 32 + kQ2Warps * i: 8 float4 per thread, so four CTAs (256 KB of loads in
+// flight) fit on an SM.  The last K tile may be partial (K % 128 columns, a
+// multiple of 16).  kCount: add the saturation count to *sat.
+constexpr int kQ2Threads = 512;
+constexpr int kQ2Warps = kQ2Threads / 32;
+constexpr int kQ2Rows = 128 / kQ2Warps;  // rows per thread
+
 template <bool kE5M2, bool kCount>
-__global__ void __launch_bounds__(256) quant_128x128_kernel(const float* __restrict__ W,
+__global__ void __launch_bounds__(kQ2Threads) quant_128x128_kernel(const float* __restrict__ W,
                                                             uint8_t* __restrict__ Q,
                                                             float* __restrict__ sW, int N,
                                                             int K, unsigned long long* sat) {
@@ -141,13 +146,13 @@ __global__ void __launch_bounds__(256) quant_128x128_kernel(const float* __restr
   const int r0 = threadIdx.x / 32;
   const size_t mat = size_t(e) * N * K;
   const bool col_in = cg * 4 < K - kb * kBlockK;  // this thread's 4 columns exist
-  __shared__ float red[8];
+  __shared__ float red[kQ2Warps];
 
-  float4 v[16];
+  float4 v[kQ2Rows];
   float amax = 0.f;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const int n = nb * 128 + r0 + 8 * i;
+  for (int i = 0; i < kQ2Rows; ++i) {
+    const int n = nb * 128 + r0 + kQ2Warps * i;
     if (n < N && col_in) {
       v[i] = __ldcs(reinterpret_cast<const float4*>(W + mat + size_t(n) * K + kb * kBlockK) + cg);
       amax = fmaxf(amax, absmax4(v[i]));
@@ -161,12 +166,12 @@ __global__ void __launch_bounds__(256) quant_128x128_kernel(const float* __restr
   __syncthreads();
   amax = red[0];
 #pragma unroll
-  for (int w = 1; w < 8; ++w) amax = fmaxf(amax, red[w]);
+  for (int w = 1; w < kQ2Warps; ++w) amax = fmaxf(amax, red[w]);
   const float s = __fdiv_rn(amax, f8_limit<kE5M2>());
   unsigned n_sat = 0;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const int n = nb * 128 + r0 + 8 * i;
+  for (int i = 0; i < kQ2Rows; ++i) {
+    const int n = nb * 128 + r0 + kQ2Warps * i;
     if (n < N && col_in) {
       uint32_t* dst = reinterpret_cast<uint32_t*>(Q + mat + size_t(n) * K + kb * kBlockK) + cg;
       *dst = amax != 0.f ? quant4<kE5M2, kCount>(v[i], s, &n_sat) : 0u;
@@ -175,14 +180,14 @@ __global__ void __launch_bounds__(256) quant_128x128_kernel(const float* __restr
   if (threadIdx.x == 0) sW[(size_t(e) * Nb + nb) * Kb + kb] = s;
   if constexpr (kCount) {
     // amax (and so every thread's path above) is uniform over the CTA
-    __shared__ unsigned cnt[8];
+    __shared__ unsigned cnt[kQ2Warps];
     n_sat = __reduce_add_sync(0xffffffffu, n_sat);
     if (cg == 0) cnt[r0] = n_sat;
     __syncthreads();
     if (threadIdx.x == 0) {
       unsigned t = 0;
 #pragma unroll
-      for (int w = 0; w < 8; ++w) t += cnt[w];
+      for (int w = 0; w < kQ2Warps; ++w) t += cnt[w];
       if (t != 0) atomicAdd(sat, (unsigned long long)t);
     }
   }
@@ -252,13 +257,13 @@ cudaError_t launch_quant_128x128(const LaunchCtx& c, const float* W, uint8_t* Q,
   const bool e5 = fmt == FP8GEMM_FMT_E5M2;
   if (sat != nullptr) {
     if (e5)
-      quant_128x128_kernel<true, true><<<grid, 256, 0, c.stream>>>(W, Q, sW, N, K, sat);
+      quant_128x128_kernel<true, true><<<grid, kQ2Threads, 0, c.stream>>>(W, Q, sW, N, K, sat);
     else
-      quant_128x128_kernel<false, true><<<grid, 256, 0, c.stream>>>(W, Q, sW, N, K, sat);
+      quant_128x128_kernel<false, true><<<grid, kQ2Threads, 0, c.stream>>>(W, Q, sW, N, K, sat);
   } else if (e5) {
-    quant_128x128_kernel<true, false><<<grid, 256, 0, c.stream>>>(W, Q, sW, N, K, nullptr);
+    quant_128x128_kernel<true, false><<<grid, kQ2Threads, 0, c.stream>>>(W, Q, sW, N, K, nullptr);
   } else {
-    quant_128x128_kernel<false, false><<<grid, 256, 0, c.stream>>>(W, Q, sW, N, K, nullptr);
+    quant_128x128_kernel<false, false><<<grid, kQ2Threads, 0, c.stream>>>(W, Q, sW, N, K, nullptr);
   }
   return cudaGetLastError();
 }
