@@ -536,7 +536,29 @@ def measure_configs(peaks, dev):
                                      "bound": "hbm",
                                      "roofline_frac": round(nb / (peaks["hbm_gbs"] * 1e9) /
                                                             (ms * 1e-3), 4)}
+    # the same with the saturation counter
+    cnt = torch.zeros(1, dtype=torch.int64, device=dev)
+    ms = time_launch(lambda: b.fp8_quant_1x128_fmt(X, "e4m3", Q=Q, sX=S, sat_count=cnt), flush)
+    res["quant_1x128_count_4096x16384"] = {"us": round(ms * 1e3, 2),
+                                           "gbs": round(nb / (ms * 1e-3) / 1e9, 1),
+                                           "bound": "hbm",
+                                           "roofline_frac": round(nb / (peaks["hbm_gbs"] * 1e9) /
+                                                                  (ms * 1e-3), 4),
+                                           "note": "fp8_quant_1x128_ex with a saturation counter"}
     del X, Q, S
+
+    # weight quantiser (the offline step) on the prefill B, 7168 x 16384
+    _, W = synthetic.dense_operands_device(8, 7168, 16384, kind="prefill", seed=0, device=dev)
+    QW = torch.empty(W.shape, dtype=torch.uint8, device=dev)
+    SW = torch.empty((56, 128), dtype=torch.float32, device=dev)
+    ms = time_launch(lambda: b.fp8_quant_128x128(W, Q=QW, sW=SW), flush)
+    nb = W.numel() * 5 + SW.numel() * 4
+    res["quant_128x128_7168x16384"] = {"us": round(ms * 1e3, 2),
+                                       "gbs": round(nb / (ms * 1e-3) / 1e9, 1),
+                                       "bound": "hbm",
+                                       "roofline_frac": round(nb / (peaks["hbm_gbs"] * 1e9) /
+                                                              (ms * 1e-3), 4)}
+    del W, QW, SW, cnt
 
     # MoE contiguous: 32 experts, 8192 Zipf(1.1) tokens, N=4096, K=7168
     E, T, N, K = 32, 8192, 4096, 7168
