@@ -361,6 +361,17 @@ int fp8gemm_dense_quant_a_ex(const float* X, uint8_t* Q, float* sA, const uint8_
       (Q && (!aligned16(Q) || !aligned16(sA))))
     return FP8GEMM_ERR_ALIGN;
   if ((long long)M * K > (1LL << 46)) return FP8GEMM_ERR_SHAPE;
+  if (M <= kSmallM) {
+    // decode sizes: one launch that quantises A on load, where the shape allows
+    LaunchCtx c;
+    if (int r = ctx_for(stream, &c)) return r;
+    GemmArgs a{GemmMode::kDense, nullptr, nullptr, B, sB, nullptr, static_cast<__nv_bfloat16*>(D),
+               M, N, K, 1};
+    a.b_read_only = (flags & FP8GEMM_FLAG_B_READ_ONLY) ? 1 : 0;
+    bool taken = false;
+    const cudaError_t e = launch_gemm_small_m_quant(c, a, X, Q, sA, &taken);
+    if (taken) return finish(e, 1);
+  }
   if (!Q) {  // quantised A in the library's buffer: bytes, then (16-B aligned) scales
     const size_t qbytes = (size_t(M) * K + 15) / 16 * 16;
     void* ws = nullptr;

@@ -83,6 +83,11 @@ size_t small_m_workspace_bytes(int num_sms, int N);
 bool small_m_uses_workspace(const LaunchCtx& c, const GemmArgs& a);
 cudaError_t launch_gemm_small_m_any(const LaunchCtx& c, const GemmArgs& a, void* ws,
                                     size_t ws_bytes);
+// The dense decode path from FP32 activations X (M <= 64), quantised on load
+// inside the GEMM, with Q / sA (both or neither) written too; *taken = false
+// when the shape does not qualify (nothing is launched).
+cudaError_t launch_gemm_small_m_quant(const LaunchCtx& c, const GemmArgs& a, const float* X,
+                                      uint8_t* Q, float* sA, bool* taken);
 
 // Many decode-sized problems from a device-resident table (gemm_table.cu),
 // K split over the CTAs (stream-K) through a zeroed workspace of

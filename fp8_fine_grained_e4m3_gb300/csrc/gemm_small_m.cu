@@ -32,7 +32,10 @@
 //
 // CTA layout (192 threads): warps 0-3 promotion/epilogue (thread = TMEM lane
 // = output column), warp 4 TMA producer, warp 5 MMA issuer.
+#include <cstring>
+
 #include "common.cuh"
+#include "f8_convert.cuh"
 #include "ptx.cuh"
 
 namespace fp8gemm {
@@ -80,11 +83,18 @@ __device__ __forceinline__ void drain_wait_sm(uint64_t* bar, uint32_t parity) {
   }
 }
 
-template <class Cfg, bool kClusterSplit>
+// kQuant (cluster form only, every CTA's K range within the stages): the
+// activations arrive as FP32 X (Xf, [M, K]) and the promotion warps quantise
+// the CTA's K blocks into the operand stages themselves -- fp8_quant_1x128's
+// arithmetic, bit for bit -- instead of the producer loading quantised ones;
+// the first tile's cluster also writes Q and sA when Qout is given.
+template <class Cfg, bool kClusterSplit, bool kQuant = false>
 __global__ void __launch_bounds__(Cfg::kThreads, 2)
     gemm_small_m_kernel(const __grid_constant__ CUtensorMap tmW,
                         const __grid_constant__ CUtensorMap tmX, const GemmArgs args,
-                        float* ws_partials, int* ws_counters, int* status, int cluster) {
+                        float* ws_partials, int* ws_counters, int* status, int cluster,
+                        const float* Xf, uint8_t* Qout, float* sAout) {
+  static_assert(!kQuant || kClusterSplit, "quantise-on-load runs in the cluster form");
   constexpr int MP = Cfg::MP;
   constexpr int kStages = Cfg::kStages;
 
@@ -101,7 +111,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 2)
   uint64_t* tempty_bar = tfull_bar + NB;
   uint64_t* drain_bar = tempty_bar + NB;
   uint64_t* group_bar = drain_bar + 1;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(group_bar + 1);
+  uint64_t* xq_bar = group_bar + 1;  // kQuant: the operand stages hold the quantised activations
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(group_bar + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_holder + 2);
   // scales of the current batch of K blocks: sa_s[q][j] = sA[j, kb + q], sb_s[q]
@@ -134,6 +145,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 2)
     }
     mbar_init(drain_bar, 1);
     mbar_init(group_bar, 128);
+    mbar_init(xq_bar, 4);  // one arrival per promotion warp
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -143,7 +155,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 2)
   }
   if (warp == Cfg::kTmaWarp && lane == 0) {
     tma_prefetch_desc(&tmW);
-    tma_prefetch_desc(&tmX);
+    if (!kQuant) tma_prefetch_desc(&tmX);  // (kQuant: tmX is not a valid map)
   }
   tc_fence_before();
   __syncthreads();
@@ -170,10 +182,12 @@ __global__ void __launch_bounds__(Cfg::kThreads, 2)
       // straight into shared memory instead: their full barriers are armed
       // for weights and activations, the activation halves follow the wait.
       const int pre = args.b_read_only ? (n_units < kStages ? n_units : kStages) : 0;
+      // bytes a stage's copies bring (kQuant: the weights only)
+      constexpr uint32_t kStageTx = Cfg::kWBytes + (kQuant ? 0 : Cfg::kXBytes);
       for (int i = 0; i < n_units; ++i) {
         const long long u = u_begin + i;
         if (i < pre) {  // first use of each stage: nothing to wait for
-          mbar_arrive_expect_tx(&full_bar[i], Cfg::kWBytes + Cfg::kXBytes);
+          mbar_arrive_expect_tx(&full_bar[i], kStageTx);
           tma_load_2d_hint(smW + i * Cfg::kWBytes, &tmW, &full_bar[i], int(u % Kb) * kBlockK,
                            int(u / Kb) * 128, pol_stream);
         } else {
@@ -181,9 +195,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 2)
         }
       }
       griddep_wait();
-      for (int i = 0; i < pre; ++i)
-        tma_load_2d_hint(smX + i * Cfg::kXBytes, &tmX, &full_bar[i],
-                         int((u_begin + i) % Kb) * kBlockK, 0, pol_keep);
+      if (!kQuant)
+        for (int i = 0; i < pre; ++i)
+          tma_load_2d_hint(smX + i * Cfg::kXBytes, &tmX, &full_bar[i],
+                           int((u_begin + i) % Kb) * kBlockK, 0, pol_keep);
       int i = pre;
       for (; i < n_units; ++i) {
         const long long u = u_begin + i;
@@ -193,11 +208,12 @@ __global__ void __launch_bounds__(Cfg::kThreads, 2)
           fail();
           break;
         }
-        mbar_arrive_expect_tx(&full_bar[s], Cfg::kWBytes + Cfg::kXBytes);
+        mbar_arrive_expect_tx(&full_bar[s], kStageTx);
         tma_load_2d_hint(smW + s * Cfg::kWBytes, &tmW, &full_bar[s], int(u % Kb) * kBlockK,
                          int(u / Kb) * 128, pol_stream);
-        tma_load_2d_hint(smX + s * Cfg::kXBytes, &tmX, &full_bar[s], int(u % Kb) * kBlockK, 0,
-                         pol_keep);
+        if (!kQuant)
+          tma_load_2d_hint(smX + s * Cfg::kXBytes, &tmX, &full_bar[s], int(u % Kb) * kBlockK, 0,
+                           pol_keep);
       }
       const int n = i < kStages ? i : kStages;  // let in-flight copies land
       for (int j = i - n; j < i; ++j) drain_wait_sm(&full_bar[j % kStages], (j / kStages) & 1);
@@ -217,7 +233,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 2)
         const int buf = i % NB;
         const uint32_t tph = (i / NB) & 1;
         if (!mbar_wait(&tempty_bar[buf], tph ^ 1, abort_flag, args.wait_ns) ||
-            !mbar_wait(&full_bar[s], ph, abort_flag, args.wait_ns)) {
+            !mbar_wait(&full_bar[s], ph, abort_flag, args.wait_ns) ||
+            (kQuant && i == 0 && !mbar_wait(xq_bar, 0, abort_flag, args.wait_ns))) {
           fail();
           break;
         }
@@ -253,6 +270,60 @@ __global__ void __launch_bounds__(Cfg::kThreads, 2)
       return r;
     };
     griddep_wait();  // sA, the workspace and D belong to the stream's order
+    if constexpr (kQuant) {
+      // The CTA's units are K blocks kq0 .. kq0 + n_units - 1 of one tile,
+      // unit i in stage i.  Each (unit, row) pair is one 1x128 block: a lane
+      // takes 4 of its FP32 values, the warp reduces amax, s = amax / 448,
+      // the bytes go to the stage's activation slot (row j, 128-byte
+      // swizzle) and s to sa_s[i][j]; rows j >= M are zero.
+      const int kq0 = int(u_begin % Kb);
+      const int K = args.K;
+      const bool publish = Qout != nullptr && u_begin < Kb;  // the first tile's cluster
+      // rows M .. MP-1 of every unit's slot: zero bytes, zero scales
+      const int zrows = n_units * (MP - M);
+      for (int idx = warp * 32 + lane; idx < zrows * 8; idx += 128) {
+        const int zr = idx / 8, i = zr / (MP - M), j = M + zr % (MP - M);
+        *reinterpret_cast<uint4*>(smX + i * Cfg::kXBytes + j * 128 + (idx % 8) * 16) =
+            make_uint4(0u, 0u, 0u, 0u);
+        if (idx % 8 == 0) sa_s[i * MP + j] = 0.f;
+      }
+      // the M real rows: pair p = (unit p / M, row p % M), 8 pairs per warp
+      // per round with every load in flight before the first is used
+      const int pairs = n_units * M;
+      for (int p0 = warp * 8; p0 < pairs; p0 += 32) {
+        float4 v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int p = p0 + e, i = p / M, j = p % M, kb = kq0 + i;
+          const bool in = p < pairs && lane * 4 < K - kb * kBlockK;
+          v[e] = in ? __ldg(reinterpret_cast<const float4*>(Xf + size_t(j) * K +
+                                                            size_t(kb) * kBlockK) + lane)
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int p = p0 + e, i = p / M, j = p % M, kb = kq0 + i;
+          if (p >= pairs) break;  // warp-uniform
+          float amax = absmax4(v[e]);
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1)
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+          const float sq = __fdiv_rn(amax, f8_limit<false>());
+          const uint32_t q = amax != 0.f ? quant4<false>(v[e], sq) : 0u;
+          *reinterpret_cast<uint32_t*>(smX + i * Cfg::kXBytes + j * 128 +
+                                       (((lane >> 2) ^ (j & 7)) << 4) + (lane & 3) * 4) = q;
+          if (lane == 0) sa_s[i * MP + j] = sq;
+          if (publish) {
+            if (lane * 4 < K - kb * kBlockK)
+              reinterpret_cast<uint32_t*>(Qout + size_t(j) * K + size_t(kb) * kBlockK)[lane] = q;
+            if (lane == 0) sAout[size_t(j) * Kb + kb] = sq;
+          }
+        }
+      }
+      fence_proxy_async_smem();  // the stores (generic proxy) before the MMAs read them
+      __syncwarp();
+      if (lane == 0) mbar_arrive(xq_bar);
+    }
     int it = 0;
     for (long long u = u_begin; u < u_end && ok;) {
       const int tile = int(u / Kb);
@@ -270,10 +341,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, 2)
           // loads (one latency per batch, not one per K block)
           const int nkb = min(Cfg::kScaleKb, kb1 - kb);
           if (!group_sync()) { fail(); ok = false; break; }  // previous batch consumed
-          for (int idx = t; idx < MP * nkb; idx += 128) {
-            const int j = idx / nkb, qq = idx % nkb;
-            sa_s[qq * MP + j] = j < M ? __ldg(args.sA + size_t(j) * Kb + kb + qq) : 0.f;
-          }
+          if (!kQuant)  // (kQuant: the quantisation above wrote sa_s)
+            for (int idx = t; idx < MP * nkb; idx += 128) {
+              const int j = idx / nkb, qq = idx % nkb;
+              sa_s[qq * MP + j] = j < M ? __ldg(args.sA + size_t(j) * Kb + kb + qq) : 0.f;
+            }
           if (t < nkb) sb_s[t] = __ldg(args.sB + size_t(tile) * Kb + kb + t);
           if (!group_sync()) { fail(); ok = false; break; }
         }
@@ -453,6 +525,12 @@ cudaError_t prepare_kernels(int dev) {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(gemm_small_m_kernel<Cfg, true>,
                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gemm_small_m_kernel<Cfg, true, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, int(Cfg::kSmemBytes));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gemm_small_m_kernel<Cfg, true, true>,
+                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e == cudaSuccess) done |= 1ull << (dev & 63);
   return e;
 }
@@ -554,12 +632,67 @@ cudaError_t run(const LaunchCtx& c, const GemmArgs& args, void* ws, size_t ws_by
   cfg.numAttrs = split > 0 ? 2 : 1;
   if (split > 0)
     return cudaLaunchKernelEx(&cfg, gemm_small_m_kernel<Cfg, true>, tmW, tmX, a, partials,
-                              counters, c.status, split);
+                              counters, c.status, split, (const float*)nullptr,
+                              (uint8_t*)nullptr, (float*)nullptr);
   return cudaLaunchKernelEx(&cfg, gemm_small_m_kernel<Cfg, false>, tmW, tmX, a, partials,
-                            counters, c.status, 1);
+                            counters, c.status, 1, (const float*)nullptr, (uint8_t*)nullptr,
+                            (float*)nullptr);
+}
+
+// Quantise-on-load: the cluster form when every CTA's K range fits in the
+// stages (one stage per K block, none reused), launched as a programmatic
+// dependent like run(); *taken = false leaves the call to the caller.
+template <class Cfg>
+cudaError_t run_quant(const LaunchCtx& c, const GemmArgs& args, const float* X, uint8_t* Q,
+                      float* sA, bool* taken) {
+  *taken = false;
+  GemmArgs a = args;
+  a.wait_ns = wait_limit_ns();
+  const int Kb = ceil_div(a.K, kBlockK);
+  const int n_tiles = ceil_div(a.N, 128);
+  const int split = cluster_split<Cfg>(c, n_tiles, Kb);
+  // Each (K block, row) of a CTA's range is one 1x128 block for its four
+  // promotion warps to quantise before the first MMA, on the critical path:
+  // up to 16 (a few rows) that costs less than a separate quantiser launch
+  // (1 x 7168 x 2048: 7.4 against 8.1 us); at 64 (16 rows) it costs more
+  // (11.7 against 9.0 us).
+  const int units = split < 1 ? 0 : ceil_div(Kb, split);
+  if (split < 1 || units > Cfg::kStages || units * a.M > 16) return cudaSuccess;
+  *taken = true;
+  CUtensorMap tmW, tmX;
+  if (!make_tmap_u8_sw128(&tmW, a.B, uint64_t(a.N), a.K, 128)) return cudaErrorInvalidValue;
+  memset(&tmX, 0, sizeof(tmX));  // activations come from X, not through a tensor map
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (cudaError_t e = prepare_kernels<Cfg>(dev)) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_tiles * split);
+  cfg.blockDim = dim3(Cfg::kThreads);
+  cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+  cfg.stream = c.stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = split;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, gemm_small_m_kernel<Cfg, true, true>, tmW, tmX, a,
+                            (float*)nullptr, (int*)nullptr, c.status, split, X, Q, sA);
 }
 
 }  // namespace
+
+cudaError_t launch_gemm_small_m_quant(const LaunchCtx& c, const GemmArgs& a, const float* X,
+                                      uint8_t* Q, float* sA, bool* taken) {
+  *taken = false;
+  if (a.M < 1 || a.M > kMaxMP) return cudaSuccess;
+  if (a.M <= 16) return run_quant<SmCfg<16>>(c, a, X, Q, sA, taken);
+  if (a.M <= 32) return run_quant<SmCfg<32>>(c, a, X, Q, sA, taken);
+  return run_quant<SmCfg<64>>(c, a, X, Q, sA, taken);
+}
 
 size_t small_m_workspace_bytes(int num_sms, int /*N*/) {
   return size_t(kCounterBytes) + size_t(2) * num_sms * kMaxMP * 128 * 4;

@@ -226,11 +226,17 @@ int fp8gemm_dense_ex(const uint8_t* A, const float* sA, int a_fmt, const uint8_t
  *   D  bf16 [M, N] (output, written in full)
  *   M, N >= 0; K > 0, K % 16 == 0; all pointers 16-B aligned.
  *
- * Two kernels on `stream`: the quantiser, then the GEMM launched as its
- * programmatic dependent, so the GEMM's launch, prologue and weight prefetch
- * overlap the quantiser.  With Q/sA NULL the quantised A lives in a
- * library-owned per-stream buffer of about M*K*(1 + 4/128) bytes.  Exactly
- * one of Q, sA NULL returns FP8GEMM_ERR_NULL.
+ * A few rows (decode shapes where each CTA of the cluster split-K form has at
+ * most 16 1x128 blocks of A to quantise, e.g. M <= 4 at K = 2048): one
+ * kernel, whose CTAs quantise their own K range of X into their operand
+ * stages (same bytes and scales; the first N tile's CTAs also write Q/sA
+ * when given).  Otherwise two kernels on `stream`: the quantiser, then the
+ * GEMM launched as its programmatic dependent, so the GEMM's launch,
+ * prologue and weight prefetch overlap the quantiser; with Q/sA NULL the
+ * quantised A then lives in a library-owned per-stream buffer of about
+ * M*K*(1 + 4/128) bytes.  Either way D is bit-identical to
+ * fp8_quant_1x128 followed by fp8gemm_dense.  Exactly one of Q, sA NULL
+ * returns FP8GEMM_ERR_NULL.
  */
 int fp8gemm_dense_quant_a(const float* X, uint8_t* Q, float* sA, const uint8_t* B,
                           const float* sB, void* D, int M, int N, int K,

@@ -35,6 +35,12 @@ def _weights(N, K, seed):
     (200, 2304, 1024),   # large-M GEMM
     (3, 1000, 400),      # partial last K block
     (150, 333, 272),     # large M, N odd, partial K block
+    (16, 7168, 2064),    # partial last K block (17 blocks over 5-CTA clusters)
+    (48, 3000, 2064),    # 48 of 64 rows, 8-CTA clusters, partial K block
+    # quantised inside the decode GEMM (a few rows, K range within the stages)
+    (3, 7168, 2064),     # 3 of 16 rows, partial last K block, 5-CTA clusters
+    (4, 3000, 2048),     # 8-CTA clusters, 2 K blocks each
+    (2, 1536, 7168),     # 12-CTA clusters (above the portable size)
 ])
 def test_quant_a_matches_oracle_and_two_call_path(M, N, K):
     b = _b()
