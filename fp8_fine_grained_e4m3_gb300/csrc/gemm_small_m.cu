@@ -272,10 +272,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, 2)
     griddep_wait();  // sA, the workspace and D belong to the stream's order
     if constexpr (kQuant) {
       // The CTA's units are K blocks kq0 .. kq0 + n_units - 1 of one tile,
-      // unit i in stage i.  Each (unit, row) pair is one 1x128 block: a lane
-      // takes 4 of its FP32 values, the warp reduces amax, s = amax / 448,
-      // the bytes go to the stage's activation slot (row j, 128-byte
-      // swizzle) and s to sa_s[i][j]; rows j >= M are zero.
+      // unit i in stage i.  Each (unit, row) pair is one 1x128 block: an
+      // 8-lane group takes it (16 FP32 values per lane), reduces amax,
+      // s = amax / 448, and writes the bytes to the stage's activation slot
+      // (row j, 128-byte swizzle: a lane's 16 bytes are one chunk) and s to
+      // sa_s[i][j]; rows j >= M are zero.
       const int kq0 = int(u_begin % Kb);
       const int K = args.K;
       const bool publish = Qout != nullptr && u_begin < Kb;  // the first tile's cluster
@@ -287,36 +288,39 @@ __global__ void __launch_bounds__(Cfg::kThreads, 2)
             make_uint4(0u, 0u, 0u, 0u);
         if (idx % 8 == 0) sa_s[i * MP + j] = 0.f;
       }
-      // the M real rows: pair p = (unit p / M, row p % M), 8 pairs per warp
-      // per round with every load in flight before the first is used
+      // The M real rows: pair p = (unit p / M, row p % M) is one 1x128 block,
+      // taken by an 8-lane group (16 values per lane), four pairs per warp
+      // and round; K % 16 == 0, so a lane's 16 values are all in or all out.
+      const int g = lane >> 3, t8 = lane & 7;
       const int pairs = n_units * M;
-      for (int p0 = warp * 8; p0 < pairs; p0 += 32) {
-        float4 v[8];
+      for (int p0 = warp * 4; p0 < pairs; p0 += 16) {
+        const int p = p0 + g, i = p / M, j = p % M, kb = kq0 + i;
+        const bool have = p < pairs;
+        const bool in = have && t8 * 16 < K - kb * kBlockK;
+        float4 v[4];
+        const float4* src =
+            reinterpret_cast<const float4*>(Xf + size_t(j) * K + size_t(kb) * kBlockK + t8 * 16);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int p = p0 + e, i = p / M, j = p % M, kb = kq0 + i;
-          const bool in = p < pairs && lane * 4 < K - kb * kBlockK;
-          v[e] = in ? __ldg(reinterpret_cast<const float4*>(Xf + size_t(j) * K +
-                                                            size_t(kb) * kBlockK) + lane)
-                    : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+        for (int c = 0; c < 4; ++c) v[c] = in ? __ldg(src + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+        float amax = fmaxf(fmaxf(absmax4(v[0]), absmax4(v[1])), fmaxf(absmax4(v[2]), absmax4(v[3])));
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int p = p0 + e, i = p / M, j = p % M, kb = kq0 + i;
-          if (p >= pairs) break;  // warp-uniform
-          float amax = absmax4(v[e]);
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1)
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-          const float sq = __fdiv_rn(amax, f8_limit<false>());
-          const uint32_t q = amax != 0.f ? quant4<false>(v[e], sq) : 0u;
-          *reinterpret_cast<uint32_t*>(smX + i * Cfg::kXBytes + j * 128 +
-                                       (((lane >> 2) ^ (j & 7)) << 4) + (lane & 3) * 4) = q;
-          if (lane == 0) sa_s[i * MP + j] = sq;
+        for (int o = 4; o > 0; o >>= 1)  // within the 8-lane group
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const float sq = __fdiv_rn(amax, f8_limit<false>());
+        const bool nz = amax != 0.f;
+        const float sd = nz ? sq : 1.f;  // no division by zero on the way to zero bytes
+        uint4 q;
+        q.x = nz ? quant4<false>(v[0], sd) : 0u;
+        q.y = nz ? quant4<false>(v[1], sd) : 0u;
+        q.z = nz ? quant4<false>(v[2], sd) : 0u;
+        q.w = nz ? quant4<false>(v[3], sd) : 0u;
+        if (have) {
+          *reinterpret_cast<uint4*>(smX + i * Cfg::kXBytes + j * 128 + ((t8 ^ (j & 7)) << 4)) = q;
+          if (t8 == 0) sa_s[i * MP + j] = sq;
           if (publish) {
-            if (lane * 4 < K - kb * kBlockK)
-              reinterpret_cast<uint32_t*>(Qout + size_t(j) * K + size_t(kb) * kBlockK)[lane] = q;
-            if (lane == 0) sAout[size_t(j) * Kb + kb] = sq;
+            if (in)
+              *reinterpret_cast<uint4*>(Qout + size_t(j) * K + size_t(kb) * kBlockK + t8 * 16) = q;
+            if (t8 == 0) sAout[size_t(j) * Kb + kb] = sq;
           }
         }
       }
@@ -652,10 +656,10 @@ cudaError_t run_quant(const LaunchCtx& c, const GemmArgs& args, const float* X, 
   const int n_tiles = ceil_div(a.N, 128);
   const int split = cluster_split<Cfg>(c, n_tiles, Kb);
   // Each (K block, row) of a CTA's range is one 1x128 block for its four
-  // promotion warps to quantise before the first MMA, on the critical path:
-  // up to 16 (a few rows) that costs less than a separate quantiser launch
-  // (1 x 7168 x 2048: 7.4 against 8.1 us); at 64 (16 rows) it costs more
-  // (11.7 against 9.0 us).
+  // promotion warps to quantise before the first MMA, on the critical path,
+  // four blocks per warp and round: up to 16 (one round) that costs less than
+  // a separate quantiser launch (1 x 7168 x 2048: 6.4 against 8.1 us); at 64
+  // (16 rows, four rounds) it costs more (9.1-9.8 against 8.9 us).
   const int units = split < 1 ? 0 : ceil_div(Kb, split);
   if (split < 1 || units > Cfg::kStages || units * a.M > 16) return cudaSuccess;
   *taken = true;
