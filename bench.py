@@ -279,14 +279,15 @@ def run_gpu(args, rank, world):
     return out
 
 
-def measure_e2e(args, cases, flops_step, world, chunks=4):
+def measure_e2e(args, cases, flops_step, world, chunks=4, parts=2):
     """The step through the public API with pinned host input and output,
     every copy inside the timed interval (CUDA events around the whole step):
     H2D of each shape's X in `chunks` row blocks on a copy stream, the 1x128
-    quantiser on each block as soon as it has landed, the GEMM, and the D2H
-    of D on a second copy stream -- so one shape's copies overlap the other's
-    kernels and the two copy directions run at once.  Steps do not overlap:
-    each ends when its last D2H has landed."""
+    quantiser on each block as soon as it has landed, the GEMM in `parts` row
+    blocks (each as soon as its rows are quantised; rows are independent, so D
+    is the same as one call's), and the D2H of each part on a second copy
+    stream -- so copies overlap kernels and the two copy directions run at
+    once.  Steps do not overlap: each ends when its last D2H has landed."""
     import torch
 
     from fp8_fine_grained_e4m3_gb300 import binding as b
@@ -322,27 +323,39 @@ def measure_e2e(args, cases, flops_step, world, chunks=4):
                 landed.append(evs)
         last = None
         for c, (_, Dh), evs in zip(cases, hosts, landed):
-            for r0, r1, ev in evs:
-                cur.wait_event(ev)
-                b.fp8_quant_1x128(c["X"][r0:r1], Q=c["A8"][r0:r1], sX=c["sA"][r0:r1])
-            b.fp8gemm_dense(c["A8"], c["sA"], c["B8"], c["sB"], D=c["D"])
-            done = torch.cuda.Event()
-            done.record(cur)
-            s_out.wait_event(done)
-            with torch.cuda.stream(s_out):
-                Dh.copy_(c["D"], non_blocking=True)
-                last = torch.cuda.Event()
-                last.record(s_out)
+            M = c["X"].shape[0]
+            per = chunks // parts
+            for q in range(parts):
+                for r0, r1, ev in evs[q * per:(q + 1) * per]:
+                    cur.wait_event(ev)
+                    b.fp8_quant_1x128(c["X"][r0:r1], Q=c["A8"][r0:r1], sX=c["sA"][r0:r1])
+                g0, g1 = evs[q * per][0], evs[(q + 1) * per - 1][1]
+                b.fp8gemm_dense(c["A8"][g0:g1], c["sA"][g0:g1], c["B8"], c["sB"],
+                                D=c["D"][g0:g1])
+                done = torch.cuda.Event()
+                done.record(cur)
+                s_out.wait_event(done)
+                with torch.cuda.stream(s_out):
+                    Dh[g0:g1].copy_(c["D"][g0:g1], non_blocking=True)
+                    last = torch.cuda.Event()
+                    last.record(s_out)
         cur.wait_event(last)
         e.record(cur)
         e.synchronize()
         if i >= 2:
             times.append(s.elapsed_time(e))
     ms = sum(times) / len(times)
+    # the result of the timed path equals one-call results
+    ref = [(c["D"].clone()) for c in cases]
+    for c, r in zip(cases, ref):
+        b.fp8gemm_dense(c["A8"], c["sA"], c["B8"], c["sB"], D=c["D"])
+        if not torch.equal(c["D"], r):
+            raise RuntimeError("row-block GEMMs differ from the one-call result")
     return {"value": round(world * flops_step / (ms * 1e-3) / 1e12, 2), "unit": UNIT,
             "ms_per_step": round(ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": n, "overlap": f"H2D in {chunks} row blocks per shape, quantiser per block, "
-                                   "D2H on a second copy stream"}
+                                   f"GEMM in {parts} row blocks, D2H of each on a second copy "
+                                   "stream"}
 
 
 def time_launch(fn, flush, n=20, warm=3):
