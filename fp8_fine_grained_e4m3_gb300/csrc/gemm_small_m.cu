@@ -76,6 +76,58 @@ struct StreamK {
   __device__ int cta_of(long long u) const { return int(((u + 1) * G - 1) / U); }
 };
 
+// Cluster split-K reduction of rows j0, j0 + 4, ... (< r1) of 4 adjacent
+// columns col4 .. col4 + 3 (lane c4 of the 128-column partials at `part` in
+// the shared memory of ranks 0..C-1), summed in rank order (= K order:
+// deterministic) and written to D as BF16; kRows rows a round, all of a
+// round's C x kRows 16-byte remote loads issued before any is used.
+template <int kRows, int kMaxC>
+__device__ __forceinline__ void cluster_reduce_rows4(const float* part, int C, int j0, int r1,
+                                                     int col4, int c4, const GemmArgs& args) {
+  const float4* src[kMaxC];
+#pragma unroll
+  for (int r = 0; r < kMaxC; ++r)
+    src[r] = reinterpret_cast<const float4*>(map_shared_rank(part, uint32_t(r < C ? r : 0))) + c4;
+  const bool vec_ok = args.N % 4 == 0 && col4 + 3 < args.N;
+  for (int j = j0; j < r1; j += 4 * kRows) {
+    float4 v[kRows][kMaxC];
+#pragma unroll
+    for (int q = 0; q < kRows; ++q)
+#pragma unroll
+      for (int r = 0; r < kMaxC; ++r)
+        v[q][r] = (r < C && j + 4 * q < r1) ? src[r][(j + 4 * q) * 32]
+                                            : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < kRows; ++q) {
+      const int row = j + 4 * q;
+      if (row >= r1) continue;
+      float4 sum = v[q][0];
+#pragma unroll
+      for (int r = 1; r < kMaxC; ++r)
+        if (r < C) {
+          sum.x += v[q][r].x;
+          sum.y += v[q][r].y;
+          sum.z += v[q][r].z;
+          sum.w += v[q][r].w;
+        }
+      __nv_bfloat16* d = args.D + size_t(row) * args.N + col4;
+      const __nv_bfloat162 lo = __float22bfloat162_rn(make_float2(sum.x, sum.y));
+      const __nv_bfloat162 hi = __float22bfloat162_rn(make_float2(sum.z, sum.w));
+      if (vec_ok) {
+        uint2 u;
+        u.x = *reinterpret_cast<const uint32_t*>(&lo);
+        u.y = *reinterpret_cast<const uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(d) = u;
+      } else {
+        if (col4 < args.N) d[0] = lo.x;
+        if (col4 + 1 < args.N) d[1] = lo.y;
+        if (col4 + 2 < args.N) d[2] = hi.x;
+        if (col4 + 3 < args.N) d[3] = hi.y;
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ void drain_wait_sm(uint64_t* bar, uint32_t parity) {
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {
@@ -476,33 +528,17 @@ __global__ void __launch_bounds__(Cfg::kThreads, 2)
     cluster_sync();
     if (warp < 4) {
       // this CTA sums rows [r0, r1) of the tile over the partials of ranks
-      // 0..C-1 in rank order (= K order: deterministic)
-      const int t = threadIdx.x;
+      // 0..C-1 in rank order (= K order: deterministic); a thread takes 4
+      // adjacent columns (16-byte loads through distributed shared memory)
       const int C = cluster;
       const int M = args.M;
       const int r0 = crank * M / C, r1 = (crank + 1) * M / C;
-      const int col = int(blockIdx.x) / C * 128 + t;
+      const int col4 = int(blockIdx.x) / C * 128 + (lane << 2);
       const float* part = reinterpret_cast<const float*>(smW);
-      const float* src[kMaxCluster];
-#pragma unroll
-      for (int r = 0; r < kMaxCluster; ++r) src[r] = map_shared_rank(part, uint32_t(r < C ? r : 0));
-      for (int j = r0; j < r1; j += 4) {
-        float v[4][kMaxCluster];
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-#pragma unroll
-          for (int r = 0; r < kMaxCluster; ++r)
-            v[q][r] = (r < C && j + q < r1) ? src[r][(j + q) * 128 + t] : 0.f;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float sum = v[q][0];
-#pragma unroll
-          for (int r = 1; r < kMaxCluster; ++r)
-            if (r < C) sum += v[q][r];
-          if (j + q < r1 && col < args.N)
-            args.D[size_t(j + q) * args.N + col] = __float2bfloat16_rn(sum);
-        }
-      }
+      if (C <= 8)
+        cluster_reduce_rows4<2, 8>(part, C, r0 + warp, r1, col4, lane, args);
+      else
+        cluster_reduce_rows4<1, kMaxCluster>(part, C, r0 + warp, r1, col4, lane, args);
     }
     __syncwarp();
     cluster_sync();  // the partners are done reading this CTA's partial
