@@ -81,24 +81,33 @@ def fp8_peak(peaks, sustained=True):
 
 # ----------------------------------------------------------------- clocks
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples (every 10 ms) of SM clock, power and throttle
+    reasons.  `window(t0, t1)` marks the timed interval (host epoch seconds);
+    the summary is taken over the samples stamped inside it, or over all of
+    them when none fell inside (a very short interval)."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
         self.file = None
+        self.t0 = self.t1 = None
 
     def start(self):
         try:
             self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "10"],
                 stdout=self.file, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+
+    def window(self, t0, t1):
+        self.t0, self.t1 = t0, t1
 
     def stop(self):
         if self.proc is None:
@@ -110,23 +119,36 @@ class ClockSampler:
             self.proc.kill()
         self.file.flush()
         self.file.seek(0)
-        rows = [r.strip().split(", ") for r in self.file.read().splitlines() if r.strip()]
+        text = self.file.read()
         self.file.close()
         os.unlink(self.file.name)
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
+        return self.summarise(text, self.t0, self.t1)
+
+    @classmethod
+    def summarise(cls, text, t0=None, t1=None):
+        """Median SM clock, max clock and active reasons of the CSV rows in
+        [t0, t1] (every row when t0 is None or no row falls inside)."""
+        from datetime import datetime
+        rows = []
+        for line in text.splitlines():
+            r = [x.strip() for x in line.split(",")]
             try:
-                sm.append(float(r[1]))
-                smax.append(float(r[2]))
+                ts = datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(r[2]), float(r[3]), r[6:10]))
             except (ValueError, IndexError):
                 continue
-            for name, v in zip(names, r[5:9]):
-                if v.strip().lower() == "active":
+        inside = [x for x in rows if t0 is not None and t0 <= x[0] <= t1]
+        use = inside or rows
+        reasons = set()
+        for _, _, _, flags in use:
+            for name, v in zip(cls.REASONS, flags):
+                if v.lower() == "active":
                     reasons.add(name)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+        return {"sm_mhz": statistics.median(x[1] for x in use) if use else None,
+                "sm_max_mhz": max(x[2] for x in use) if use else None,
+                "samples": len(inside), "samples_total": len(rows),
+                "window_ms": round((t1 - t0) * 1e3, 1) if t0 is not None else None,
+                "reasons": sorted(reasons)}
 
 
 # ------------------------------------------------------------- GPU arm
@@ -212,12 +234,14 @@ def run_gpu(args, rank, world):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    t_begin = time.time()
     for i in range(K_steps):
         flush(i)  # L2 flush, outside the timed interval
         ev[i][0].record(stream)
         step(gev[i])
         ev[i][1].record(stream)
     torch.cuda.synchronize()
+    clocks.window(t_begin, time.time())
     if world > 1:
         torch.distributed.barrier()
     launches = b.num_kernel_launches() - launches0

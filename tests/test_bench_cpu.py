@@ -87,3 +87,29 @@ def test_traffic_figure_only_for_the_source_it_was_taken_on(tmp_path, monkeypatc
     assert bench.traffic_from_profiles("other") is None
     (csrc / "k.cu").write_text("kernel v2\n")
     assert bench.traffic_from_profiles("case") is None
+
+
+def test_clock_summary_keeps_the_timed_window():
+    """Only samples stamped inside the timed interval count; an idle sample
+    before it (low clock) and a throttled one after it are left out."""
+    import bench
+    from datetime import datetime
+    rows = [
+        "2026/01/05 10:00:00.100, 0, 345, 2070, 120.5, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "2026/01/05 10:00:00.210, 0, 2070, 2070, 900.1, 0x4, Not Active, Not Active, Not Active, Active",
+        "2026/01/05 10:00:00.220, 0, 2055, 2070, 910.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "2026/01/05 10:00:00.230, 0, 2070, 2070, 905.2, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "2026/01/05 10:00:00.400, 0, 1500, 2070, 1300.0, 0x20, Not Active, Active, Not Active, Not Active",
+        "not a row",
+    ]
+    t = lambda s: datetime.strptime(s, "%Y/%m/%d %H:%M:%S.%f").timestamp()
+    s = bench.ClockSampler.summarise("\n".join(rows), t("2026/01/05 10:00:00.200"),
+                                     t("2026/01/05 10:00:00.300"))
+    assert s["samples"] == 3 and s["samples_total"] == 5
+    assert s["sm_mhz"] == 2070.0 and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap"]
+    # no sample inside a very short window: the whole record is summarised
+    s = bench.ClockSampler.summarise("\n".join(rows), t("2026/01/05 10:00:00.300"),
+                                     t("2026/01/05 10:00:00.301"))
+    assert s["samples"] == 0 and s["samples_total"] == 5
+    assert s["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
