@@ -127,3 +127,44 @@ def test_quant_128x128_saturation_count(E, N, K, fmt):
     assert int(cnt.item()) == want
     assert np.array_equal(host(Q), host(Q0))
     assert np.array_equal(host(S).view(np.uint32), host(S0).view(np.uint32))
+
+
+@pytest.mark.parametrize("E,N,K,fmt", [(1, 256, 512, "e4m3"), (2, 300, 400, "e4m3"),
+                                       (1, 256, 256, "e5m2")])
+def test_quant_128x128_quotients_near_rounding_points(E, N, K, fmt):
+    """Weights whose quotients x / s sit within 8 ulps of every FP8 value and
+    midpoint, per 128 x 128 tile: the plain instance takes the reciprocal
+    shortcut only where it is exact and divides the rest -- bytes and scales
+    equal the oracle's, and those of the counting instance (which divides)."""
+    import torch
+    from oracle import e4m3, e5m2
+    b = _binding()
+    mod, limit = (e4m3, 448.0) if fmt == "e4m3" else (e5m2, 57344.0)
+    lut = mod.decode_table()
+    vals = np.unique(np.abs(lut[np.isfinite(lut)]))
+    vals = vals[vals <= limit]
+    points = np.concatenate([vals, (vals[1:] + vals[:-1]) / 2.0])
+    points = points[points < limit]
+    g = np.random.default_rng(E * 1000 + N + K)
+    W = np.zeros((E, N, K), np.float32)
+    for e in range(E):
+        for n0 in range(0, N, 128):
+            for k0 in range(0, K, 128):
+                rows, cols = min(128, N - n0), min(128, K - k0)
+                amax = np.float32(g.uniform(0.25, 4.0))
+                s = np.float32(amax / np.float32(limit))
+                q = g.choice(points, (rows, cols)) * g.choice([-1.0, 1.0], (rows, cols))
+                q = q * (1.0 + g.integers(-8, 9, (rows, cols)) * 2.0 ** -23)
+                t = np.clip((q * np.float64(s)).astype(np.float32), -amax, amax)
+                t[0, 0] = amax
+                W[e, n0:n0 + rows, k0:k0 + cols] = t
+    Q, S = b.fp8_quant_128x128_fmt(dev(W), fmt)
+    cnt = torch.zeros(1, dtype=torch.int64, device="cuda")
+    Qc, Sc = b.fp8_quant_128x128_fmt(dev(W), fmt, sat_count=cnt)
+    for e in range(E):
+        Qo, So = oquant.quant_128x128(W[e], fmt=fmt)
+        assert np.array_equal(host(Q)[e], Qo)
+        assert np.array_equal(host(S)[e].view(np.uint32), So.view(np.uint32))
+    assert np.array_equal(host(Q), host(Qc))
+    assert np.array_equal(host(S).view(np.uint32), host(Sc).view(np.uint32))
+    assert int(cnt.item()) == oquant.saturations_128x128(W, fmt)
