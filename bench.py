@@ -303,15 +303,18 @@ def run_gpu(args, rank, world):
     return out
 
 
-def measure_e2e(args, cases, flops_step, world, chunks=4, parts=2):
+def measure_e2e(args, cases, flops_step, world, chunks=4):
     """The step through the public API with pinned host input and output,
     every copy inside the timed interval (CUDA events around the whole step):
     H2D of each shape's X in `chunks` row blocks on a copy stream, the 1x128
-    quantiser on each block as soon as it has landed, the GEMM in `parts` row
-    blocks (each as soon as its rows are quantised; rows are independent, so D
-    is the same as one call's), and the D2H of each part on a second copy
-    stream -- so copies overlap kernels and the two copy directions run at
-    once.  Steps do not overlap: each ends when its last D2H has landed."""
+    quantiser on each block as soon as it has landed, the GEMM in row parts
+    (each as soon as its rows are quantised; rows are independent, so D is the
+    same as one call's), and the D2H of each part on a second copy stream --
+    so copies overlap kernels and the two copy directions run at once.  A
+    shape takes as many parts (dividing `chunks`) as still leave each part at
+    least a wave of whole 128 x 256 tiles: a smaller part would take the
+    split-tile form, whose K order, and so its rounding, differs from one
+    call's.  Steps do not overlap: each ends when its last D2H has landed."""
     import torch
 
     from fp8_fine_grained_e4m3_gb300 import binding as b
@@ -326,6 +329,12 @@ def measure_e2e(args, cases, flops_step, world, chunks=4, parts=2):
         hosts.append((Xh, Dh))
         h2d += Xh.numel() * 4
         d2h += Dh.numel() * 2
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    n_parts = []
+    for c in cases:
+        M, N = c["D"].shape
+        n_parts.append(max(p for p in range(1, chunks + 1) if chunks % p == 0 and
+                           (M // p) // 128 * -(-N // 256) >= sms or p == 1))
     n = max(3, min(args.steps, 20))
     times = []
     for i in range(n + 2):
@@ -346,8 +355,7 @@ def measure_e2e(args, cases, flops_step, world, chunks=4, parts=2):
                     evs.append((r0, r1, ev))
                 landed.append(evs)
         last = None
-        for c, (_, Dh), evs in zip(cases, hosts, landed):
-            M = c["X"].shape[0]
+        for c, (_, Dh), evs, parts in zip(cases, hosts, landed, n_parts):
             per = chunks // parts
             for q in range(parts):
                 for r0, r1, ev in evs[q * per:(q + 1) * per]:
@@ -378,8 +386,8 @@ def measure_e2e(args, cases, flops_step, world, chunks=4, parts=2):
     return {"value": round(world * flops_step / (ms * 1e-3) / 1e12, 2), "unit": UNIT,
             "ms_per_step": round(ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": n, "overlap": f"H2D in {chunks} row blocks per shape, quantiser per block, "
-                                   f"GEMM in {parts} row blocks, D2H of each on a second copy "
-                                   "stream"}
+                                   f"GEMM in {'/'.join(map(str, n_parts))} row blocks, D2H of "
+                                   "each on a second copy stream"}
 
 
 def time_launch(fn, flush, n=20, warm=3):
