@@ -798,6 +798,11 @@ def run_kernel_case(name, reps):
         else:
             del X, W
             fn = lambda: b.fp8gemm_dense(A8, sA, B8, sB, D=D)  # noqa: E731
+    elif name == "quant_w":  # the 128x128 weight quantiser on 7168 x 16384
+        W = synthetic.expert_weights_device(1, 7168, 16384, seed=0, device=dev)[0]
+        QW = torch.empty(W.shape, dtype=torch.uint8, device=dev)
+        SW = torch.empty((56, 128), dtype=torch.float32, device=dev)
+        fn = lambda: b.fp8_quant_128x128(W, Q=QW, sW=SW)  # noqa: E731
     elif name == "table":
         E, M_max, N, K = 16, 16, 4096, 7168
         mm = (synthetic.masked_counts(E, M_max - 1, seed=3) + 1).astype("int32")

@@ -90,18 +90,22 @@ __global__ void __launch_bounds__(256) quant_1x128_kernel(const float* __restric
 
 // One CTA (kQ2Threads threads) per 128x128 tile of one [N, K] matrix of the
 // batch.  Thread t covers column group t % 32 (4 columns) of rows
-// t / 32 + kQ2Warps * i: 8 float4 per thread, so four CTAs (256 KB of loads in
-// flight) fit on an SM.  The last K tile may be partial (K % 128 columns, a
-// multiple of 16).  kCount: add the saturation count to *sat.
+// t / 32 + kQ2Warps * i (8 float4).  The FP32 tile (64 KB) is copied into
+// shared memory with cp.async rather than held in registers, so three CTAs
+// (192 KB of copies in flight) share an SM -- 7168 x 16384 in 94 us against
+// 141 with the tile in registers (64 registers a thread, two CTAs).  Each
+// thread reads back only the elements it copied, after its own wait.  The
+// last K tile may be partial (K % 128 columns, a multiple of 16).
+// kCount: add the saturation count to *sat.
 constexpr int kQ2Threads = 512;
 constexpr int kQ2Warps = kQ2Threads / 32;
 constexpr int kQ2Rows = 128 / kQ2Warps;  // rows per thread
 
 template <bool kE5M2, bool kCount>
-__global__ void __launch_bounds__(kQ2Threads) quant_128x128_kernel(const float* __restrict__ W,
-                                                            uint8_t* __restrict__ Q,
-                                                            float* __restrict__ sW, int N,
-                                                            int K, unsigned long long* sat) {
+__global__ void __launch_bounds__(kQ2Threads, 3) quant_128x128_kernel(const float* __restrict__ W,
+                                                               uint8_t* __restrict__ Q,
+                                                               float* __restrict__ sW, int N,
+                                                               int K, unsigned long long* sat) {
   const int Kb = ceil_div(K, kBlockK);
   const int Nb = ceil_div(N, 128);
   const int kb = blockIdx.x;
@@ -111,20 +115,22 @@ __global__ void __launch_bounds__(kQ2Threads) quant_128x128_kernel(const float* 
   const int r0 = threadIdx.x / 32;
   const size_t mat = size_t(e) * N * K;
   const bool col_in = cg * 4 < K - kb * kBlockK;  // this thread's 4 columns exist
+  extern __shared__ float4 tile4[];  // [128 rows][32 float4]
   __shared__ float red[kQ2Warps];
 
-  float4 v[kQ2Rows];
-  float amax = 0.f;
+  // the tile goes to shared memory without passing through registers; each
+  // thread later reads back only what it copied
 #pragma unroll
   for (int i = 0; i < kQ2Rows; ++i) {
     const int n = nb * 128 + r0 + kQ2Warps * i;
-    if (n < N && col_in) {
-      v[i] = __ldcs(reinterpret_cast<const float4*>(W + mat + size_t(n) * K + kb * kBlockK) + cg);
-      amax = fmaxf(amax, absmax4(v[i]));
-    } else {
-      v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+    const bool in = n < N && col_in;
+    const float* src = in ? W + mat + size_t(n) * K + kb * kBlockK + cg * 4 : W;
+    cp_async_16(smem_addr(&tile4[(r0 + kQ2Warps * i) * 32 + cg]), src, in ? 16u : 0u);
   }
+  cp_async_wait_all();
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < kQ2Rows; ++i) amax = fmaxf(amax, absmax4(tile4[(r0 + kQ2Warps * i) * 32 + cg]));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   if (cg == 0) red[r0] = amax;
@@ -133,23 +139,15 @@ __global__ void __launch_bounds__(kQ2Threads) quant_128x128_kernel(const float* 
 #pragma unroll
   for (int w = 1; w < kQ2Warps; ++w) amax = fmaxf(amax, red[w]);
   const float s = __fdiv_rn(amax, f8_limit<kE5M2>());
-  // the plain instance divides through the tile's reciprocal (quant4_recip:
-  // the same bytes; 7168 x 16384 in 118 instead of 141 us); the counting one
-  // keeps the divisions, which measured faster there (124 against 131 us)
-  const float rs = __fdiv_rn(1.0f, s);
   unsigned n_sat = 0;
 #pragma unroll
   for (int i = 0; i < kQ2Rows; ++i) {
     const int n = nb * 128 + r0 + kQ2Warps * i;
     if (n < N && col_in) {
+      const float4 v = tile4[(r0 + kQ2Warps * i) * 32 + cg];
       uint32_t* dst = reinterpret_cast<uint32_t*>(Q + mat + size_t(n) * K + kb * kBlockK) + cg;
       uint32_t q = 0u;
-      if (amax != 0.f) {
-        if constexpr (kCount)
-          q = quant4<kE5M2, kCount>(v[i], s, &n_sat);
-        else
-          q = quant4_recip<kE5M2>(v[i], s, rs);
-      }
+      if (amax != 0.f) q = quant4<kE5M2, kCount>(v, s, &n_sat);
       *dst = q;
     }
   }
@@ -231,15 +229,32 @@ cudaError_t launch_quant_128x128(const LaunchCtx& c, const float* W, uint8_t* Q,
   if (Nb > 65535 || E > 65535) return cudaErrorInvalidValue;
   dim3 grid(ceil_div(K, kBlockK), Nb, E);
   const bool e5 = fmt == FP8GEMM_FMT_E5M2;
+  constexpr int kTile = 128 * 128 * 4;  // the FP32 tile in shared memory
+  static bool attr_done = false;        // per process; the attribute is per function
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(quant_128x128_kernel<true, true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kTile);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(quant_128x128_kernel<false, true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kTile);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(quant_128x128_kernel<true, false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kTile);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(quant_128x128_kernel<false, false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kTile);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
   if (sat != nullptr) {
     if (e5)
-      quant_128x128_kernel<true, true><<<grid, kQ2Threads, 0, c.stream>>>(W, Q, sW, N, K, sat);
+      quant_128x128_kernel<true, true><<<grid, kQ2Threads, kTile, c.stream>>>(W, Q, sW, N, K, sat);
     else
-      quant_128x128_kernel<false, true><<<grid, kQ2Threads, 0, c.stream>>>(W, Q, sW, N, K, sat);
+      quant_128x128_kernel<false, true><<<grid, kQ2Threads, kTile, c.stream>>>(W, Q, sW, N, K, sat);
   } else if (e5) {
-    quant_128x128_kernel<true, false><<<grid, kQ2Threads, 0, c.stream>>>(W, Q, sW, N, K, nullptr);
+    quant_128x128_kernel<true, false><<<grid, kQ2Threads, kTile, c.stream>>>(W, Q, sW, N, K, nullptr);
   } else {
-    quant_128x128_kernel<false, false><<<grid, kQ2Threads, 0, c.stream>>>(W, Q, sW, N, K, nullptr);
+    quant_128x128_kernel<false, false><<<grid, kQ2Threads, kTile, c.stream>>>(W, Q, sW, N, K, nullptr);
   }
   return cudaGetLastError();
 }

@@ -133,9 +133,9 @@ def test_quant_128x128_saturation_count(E, N, K, fmt):
                                        (1, 256, 256, "e5m2")])
 def test_quant_128x128_quotients_near_rounding_points(E, N, K, fmt):
     """Weights whose quotients x / s sit within 8 ulps of every FP8 value and
-    midpoint, per 128 x 128 tile: the plain instance takes the reciprocal
-    shortcut only where it is exact and divides the rest -- bytes and scales
-    equal the oracle's, and those of the counting instance (which divides)."""
+    midpoint, per 128 x 128 tile (e4m3 and e5m2, two experts, a ragged N and
+    a partial K tile): bytes, scales and the saturation count equal the
+    oracle's, and the plain and counting instances agree."""
     import torch
     from oracle import e4m3, e5m2
     b = _binding()
