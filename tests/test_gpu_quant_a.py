@@ -41,6 +41,8 @@ def _weights(N, K, seed):
     (3, 7168, 2064),     # 3 of 16 rows, partial last K block, 5-CTA clusters
     (4, 3000, 2048),     # 8-CTA clusters, 2 K blocks each
     (2, 1536, 7168),     # 12-CTA clusters (above the portable size)
+    (1, 2048, 7168),     # 7 K blocks per CTA, more than the stages: quantiser, then the GEMM
+    (2, 2048, 7168),
 ])
 def test_quant_a_matches_oracle_and_two_call_path(M, N, K):
     b = _b()
@@ -98,7 +100,8 @@ def test_quant_a_rejects_half_given_outputs():
         b.fp8gemm_dense_quant_a(X, B, sB, Q=Q)
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 7168, 2048), (16, 2048, 7168), (33, 1000, 1280)])
+@pytest.mark.parametrize("M,N,K", [(1, 7168, 2048), (16, 2048, 7168), (33, 1000, 1280),
+                                   (1, 2048, 7168)])
 def test_quant_a_read_only_weights_chain(M, N, K):
     """fp8gemm_dense_quant_a_ex with FLAG_B_READ_ONLY: the GEMM stages its
     weights while the quantiser (its predecessor in the stream) runs; the
