@@ -551,11 +551,14 @@ __global__ void __launch_bounds__(Cfg::kThreads, 2)
   }
 }
 
-// Sets the kernels' launch attributes once per device.
+// Sets the kernels' launch attributes once per device and context (they
+// belong to the functions in one context; a cudaDeviceReset gives the device
+// a new one).
 template <class Cfg>
 cudaError_t prepare_kernels(int dev) {
-  static unsigned long long done = 0;  // one bit per device
-  if (done >> (dev & 63) & 1ull) return cudaSuccess;
+  static unsigned long long set_in[64] = {};  // context id, per device
+  const unsigned long long ctx = current_context_id();
+  if (ctx != 0 && set_in[dev & 63] == ctx) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(gemm_small_m_kernel<Cfg, false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        int(Cfg::kSmemBytes));
@@ -571,7 +574,7 @@ cudaError_t prepare_kernels(int dev) {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(gemm_small_m_kernel<Cfg, true, true>,
                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  if (e == cudaSuccess) done |= 1ull << (dev & 63);
+  if (e == cudaSuccess) set_in[dev & 63] = ctx;
   return e;
 }
 

@@ -530,15 +530,18 @@ cudaError_t run(const LaunchCtx& c, const fp8gemm_problem* tab, int P, int max_M
   if (ws_bytes < workspace_bytes<Cfg>(c)) return cudaErrorInvalidValue;
   int* counters = static_cast<int*>(ws);
   float* partials = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + counter_bytes(c));
-  static unsigned long long attr_done = 0;  // one bit per device
+  // once per device and context: the attribute belongs to the function in
+  // one context, and a cudaDeviceReset gives the device a new one
+  static unsigned long long set_in[64] = {};  // context id, per device
   int dev = 0;
   cudaGetDevice(&dev);
-  if (!(attr_done >> (dev & 63) & 1ull)) {
+  const unsigned long long ctx = current_context_id();
+  if (ctx == 0 || set_in[dev & 63] != ctx) {
     cudaError_t e = cudaFuncSetAttribute(gemm_table_kernel<Cfg>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(Cfg::kSmemBytes));
     if (e != cudaSuccess) return e;
-    attr_done |= 1ull << (dev & 63);
+    set_in[dev & 63] = ctx;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(c.num_sms * Cfg::kCtasPerSm);

@@ -559,12 +559,17 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 
 template <class Cfg, bool kSplit>
 cudaError_t set_smem_attr() {
-  static bool done = false;  // per process; the attribute is per function
-  if (done) return cudaSuccess;
+  // once per device and context: the attribute belongs to the function in
+  // one context, and a cudaDeviceReset gives the device a new one
+  static unsigned long long set_in[64] = {};  // context id, per device
+  int dev = 0;
+  if (cudaError_t e = cudaGetDevice(&dev)) return e;
+  const unsigned long long ctx = current_context_id();
+  if (ctx != 0 && set_in[dev & 63] == ctx) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<Cfg, kSplit>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        int(Cfg::kSmemBytes));
-  if (e == cudaSuccess) done = true;
+  if (e == cudaSuccess) set_in[dev & 63] = ctx;
   return e;
 }
 

@@ -230,8 +230,13 @@ cudaError_t launch_quant_128x128(const LaunchCtx& c, const float* W, uint8_t* Q,
   dim3 grid(ceil_div(K, kBlockK), Nb, E);
   const bool e5 = fmt == FP8GEMM_FMT_E5M2;
   constexpr int kTile = 128 * 128 * 4;  // the FP32 tile in shared memory
-  static bool attr_done = false;        // per process; the attribute is per function
-  if (!attr_done) {
+  // once per device and context: the attribute belongs to the function in
+  // one context, and a cudaDeviceReset gives the device a new one
+  static unsigned long long set_in[64] = {};  // context id, per device
+  int dev = 0;
+  if (cudaError_t e = cudaGetDevice(&dev)) return e;
+  const unsigned long long ctx = current_context_id();
+  if (ctx == 0 || set_in[dev & 63] != ctx) {
     cudaError_t e = cudaFuncSetAttribute(quant_128x128_kernel<true, true>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kTile);
     if (e == cudaSuccess)
@@ -244,7 +249,7 @@ cudaError_t launch_quant_128x128(const LaunchCtx& c, const float* W, uint8_t* Q,
       e = cudaFuncSetAttribute(quant_128x128_kernel<false, false>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, kTile);
     if (e != cudaSuccess) return e;
-    attr_done = true;
+    set_in[dev & 63] = ctx;
   }
   if (sat != nullptr) {
     if (e5)
