@@ -303,6 +303,14 @@ def run_gpu(args, rank, world):
     return out
 
 
+def gemm_parts(M, N, chunks, sms):
+    """Row parts for an M x N output whose activations land in `chunks` row
+    blocks: the most (a divisor of `chunks`) that still leave every part at
+    least a wave of whole 128 x 256 tiles over `sms` SMs, else 1."""
+    return max(p for p in range(1, chunks + 1)
+               if p == 1 or (chunks % p == 0 and (M // p) // 128 * -(-N // 256) >= sms))
+
+
 def measure_e2e(args, cases, flops_step, world, chunks=4):
     """The step through the public API with pinned host input and output,
     every copy inside the timed interval (CUDA events around the whole step):
@@ -330,11 +338,7 @@ def measure_e2e(args, cases, flops_step, world, chunks=4):
         h2d += Xh.numel() * 4
         d2h += Dh.numel() * 2
     sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-    n_parts = []
-    for c in cases:
-        M, N = c["D"].shape
-        n_parts.append(max(p for p in range(1, chunks + 1) if chunks % p == 0 and
-                           (M // p) // 128 * -(-N // 256) >= sms or p == 1))
+    n_parts = [gemm_parts(*c["D"].shape, chunks, sms) for c in cases]
     n = max(3, min(args.steps, 20))
     times = []
     for i in range(n + 2):

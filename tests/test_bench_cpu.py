@@ -113,3 +113,20 @@ def test_clock_summary_keeps_the_timed_window():
                                      t("2026/01/05 10:00:00.301"))
     assert s["samples"] == 0 and s["samples_total"] == 5
     assert s["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
+
+
+def test_end_to_end_gemm_parts_keep_whole_tile_waves():
+    """The end-to-end step splits each shape's GEMM into row parts only as far
+    as every part keeps a wave of whole 128 x 256 tiles (smaller parts would
+    take the split-tile form, whose rounding differs from one call's)."""
+    import bench
+    assert bench.gemm_parts(4096, 7168, 4, 152) == 4   # 8 x 28 = 224 tiles per part
+    assert bench.gemm_parts(4096, 4096, 4, 152) == 2   # 16 x 16 = 256; 4 parts: 128 < 152
+    assert bench.gemm_parts(4096, 7168, 8, 152) == 4   # 8 parts: 4 x 28 = 112 < 152
+    assert bench.gemm_parts(1024, 4096, 4, 152) == 1   # not even one wave: one call
+    assert bench.gemm_parts(4096, 4096, 3, 152) == 3   # 1365 rows: 10 whole M blocks x 16 = 160
+    assert bench.gemm_parts(4096, 4096, 3, 168) == 1   # 160 < 168; 2 does not divide 3 blocks
+    for M, N, chunks, sms in [(4096, 7168, 4, 160), (8192, 4096, 8, 152), (4096, 4096, 4, 132)]:
+        p = bench.gemm_parts(M, N, chunks, sms)
+        assert chunks % p == 0
+        assert p == 1 or (M // p) // 128 * -(-N // 256) >= sms
