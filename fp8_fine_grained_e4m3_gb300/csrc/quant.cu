@@ -36,8 +36,9 @@ constexpr int kQuantUnroll = 4;  // 1x128 blocks per warp (loads kept in flight)
 // sX[b].  When K is a multiple of 128 (kRagged false) block b is simply
 // elements [128 b, 128 b + 128); otherwise a row's last block holds the
 // K % 128 remaining elements (a multiple of 16) and its amax runs over those.
-// kPdl: launched as a programmatic dependent of the previous kernel (wait for
-// it before the first load; let the next kernel launch right away).
+// kPdl: launched as a programmatic dependent of the previous kernel (let the
+// next kernel launch at once, then wait for the previous one before the first
+// load).
 // kCount: add the saturation count to *sat.
 template <bool kPdl, bool kRagged, bool kE5M2, bool kCount>
 __global__ void __launch_bounds__(256) quant_1x128_kernel(const float* __restrict__ X,
@@ -49,8 +50,11 @@ __global__ void __launch_bounds__(256) quant_1x128_kernel(const float* __restric
       ((long long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32) * kQuantUnroll;
   const int lane = threadIdx.x % 32;
   if constexpr (kPdl) {
-    griddep_wait();
+    // the next kernel may launch before this one's own wait: it still waits
+    // for this grid's completion (and so for the kernel before it) before it
+    // reads what this one writes
     griddep_launch_dependents();
+    griddep_wait();
   }
   float4 v[kQuantUnroll];
   long long e0[kQuantUnroll];  // first element of the block
@@ -192,9 +196,12 @@ cudaError_t launch_1x128(const LaunchCtx& c, const float* X, uint8_t* Q, float* 
     return cudaGetLastError();
   }
   // A decode-sized quantisation (one wave) is launched as a programmatic
-  // dependent of the previous kernel, so that its launch, and the prologue of
-  // the GEMM after it, overlap the kernel before.  (Not for large grids: there
-  // every short CTA would pay the dependency wait.)
+  // dependent of the previous kernel and lets the next one launch before its
+  // own wait, so that its launch, and the prologue of the GEMM after it (with
+  // read-only weights: its first weight tiles), overlap the kernel before --
+  // two launches from FP32 activations at 1 x 2048 x 7168: 8.9 -> 8.1 us,
+  // read-only 8.35 -> 7.4.  (Not for large grids: there every short CTA would
+  // pay the dependency wait.)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(grid));
   cfg.blockDim = dim3(256);
