@@ -697,8 +697,8 @@ cudaError_t run_quant(const LaunchCtx& c, const GemmArgs& args, const float* X, 
   // Each (K block, row) of a CTA's range is one 1x128 block for its four
   // promotion warps to quantise before the first MMA, on the critical path,
   // four blocks per warp and round: up to 16 (one round) that costs less than
-  // a separate quantiser launch (1 x 7168 x 2048: 6.4 against 8.1 us); at 64
-  // (16 rows, four rounds) it costs more (9.1-9.8 against 8.9 us).
+  // a separate quantiser launch (1 x 7168 x 2048: 6.3 against 7.5 us); at 64
+  // (16 rows, four rounds) it costs more (9.1-9.8 against 7.8 us).
   const int units = split < 1 ? 0 : ceil_div(Kb, split);
   if (split < 1 || units > Cfg::kStages || units * a.M > 16) return cudaSuccess;
   *taken = true;
