@@ -205,15 +205,21 @@ def run_gpu(args, rank, world):
 
     def step(gemm_events=None):
         # both quantisers first: while they run, the host enqueues the GEMMs,
-        # so the device never waits on the host inside a step
+        # so the device never waits on the host inside a step.  Then the
+        # other GEMMs, and last the dominant one (cases[0]) between the two
+        # events that time it: an event between two kernels ends the
+        # programmatic overlap of the second with the first, so only the
+        # dominant GEMM's start pays for it (its end is followed by the next
+        # step's L2 flush, not a programmatic launch)
         for c in cases:
             b.fp8_quant_1x128(c["X"], Q=c["A8"], sX=c["sA"])
-        for j, c in enumerate(cases):
-            if gemm_events is not None:
-                gemm_events[j][0].record(stream)
+        for c in cases[1:] + cases[:1]:
+            timed = gemm_events is not None and c is cases[0]
+            if timed:
+                gemm_events[0].record(stream)
             b.fp8gemm_dense(c["A8"], c["sA"], c["B8"], c["sB"], D=c["D"])
-            if gemm_events is not None:
-                gemm_events[j][1].record(stream)
+            if timed:
+                gemm_events[1].record(stream)
 
     for i in range(args.warmup):
         flush(i)
@@ -225,8 +231,8 @@ def run_gpu(args, rank, world):
     K_steps = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(K_steps)]
-    gev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in cases] for _ in range(K_steps)]
+    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K_steps)]
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
     time.sleep(0.3)
@@ -252,15 +258,14 @@ def run_gpu(args, rank, world):
 
     step_ms = [s.elapsed_time(e) for s, e in ev]
     ms_per_step = sum(step_ms) / K_steps
-    gemm_ms = [sum(g[j][0].elapsed_time(g[j][1]) for g in gev) / K_steps
-               for j in range(len(cases))]
+    gemm_ms = sum(g[0].elapsed_time(g[1]) for g in gev) / K_steps  # the dominant GEMM
     ms_per_step = max_over_ranks(ms_per_step, world)
     value = aggregate_tflops(flops_step, ms_per_step, world)
 
     # roofline of the dominant kernel: the dense GEMM on the 4096x7168x16384
-    # shape (about 80 % of the step); the other shape is listed beside it
-    gemm_flops = [2.0 * c["M"] * c["N"] * c["K"] for c in cases]
-    achieved = gemm_flops[0] / (gemm_ms[0] * 1e-3) / 1e12
+    # shape (about 70 % of the step)
+    gemm_flops = 2.0 * cases[0]["M"] * cases[0]["N"] * cases[0]["K"]
+    achieved = gemm_flops / (gemm_ms * 1e-3) / 1e12
     # each step is short (sub-ms) and starts after an L2 flush at full clock:
     # the burst figure is the denominator; the sustained one is listed beside
     peak = fp8_peak(peaks, sustained=False)
@@ -273,10 +278,7 @@ def run_gpu(args, rank, world):
                 "measured_fp8_tflops": measure_library_fp8(*PREFILL_SHAPES[0], flush),
                 "traffic": traffic_from_profiles("gemm_tc_dense_4096x7168x16384"),
                 "algorithmic_bytes": gemm_bytes(*PREFILL_SHAPES[0]),
-                "per_shape": [{"M": c["M"], "N": c["N"], "K": c["K"],
-                               "gemm_us": round(1e3 * t, 2),
-                               "tflops": round(f / (t * 1e-3) / 1e12, 1)}
-                              for c, t, f in zip(cases, gemm_ms, gemm_flops)]}
+                "gemm_us": round(1e3 * gemm_ms, 2)}
 
     # ---- end to end through the public API with host buffers
     e2e = measure_e2e(args, cases, flops_step, world)
