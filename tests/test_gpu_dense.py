@@ -3,8 +3,8 @@
 import numpy as np
 import pytest
 
-from tests.gpu_helpers import (assert_close, dev, host, ogemm, oquant, quantised_dense,
-                               sample_rows_cols)
+from tests.gpu_helpers import (assert_close, dev, host, ogemm, oquant, quant_weights,
+                               quantised_dense, sample_rows_cols)
 
 pytestmark = pytest.mark.gpu
 
@@ -118,6 +118,35 @@ def test_decode_chain_without_host_sync(M, N, K):
         refs.append(ogemm.gemm_dense(Ao, sAo, Bo, sBo))
     for got, ref in zip(outs, refs):
         assert_close(host(got), ref, f"chained decode {M}x{N}x{K}")
+    assert b.fp8gemm_get_device_status() == b.OK
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (2560, 4096, 2048),  # whole tiles after a multi-wave (plain-launch) quantiser
+    (1280, 4096, 1024),  # 160 whole tiles after a one-wave quantiser
+    (256, 4096, 4096),   # 32 tiles split along K over clusters
+    (96, 2048, 4096),    # one-wave quantiser (a programmatic dependent itself), split tiles
+])
+def test_large_m_chain_without_host_sync(M, N, K):
+    """The tensor-core GEMM is launched as a programmatic dependent of the
+    previous kernel and lets the next one launch early.  Quantise the FP32
+    activations and run the GEMM right after, three such pairs back to back,
+    with no host synchronisation in between: each GEMM must read what its
+    quantiser wrote."""
+    from fp8_fine_grained_e4m3_gb300 import synthetic
+    b = _b()
+    _, W = synthetic.dense_operands(M, N, K, kind="prefill", seed=5)
+    Bo, sBo = quant_weights(W)
+    B8, sB = dev(Bo), dev(sBo)
+    outs, xs = [], []
+    for seed in (31, 32, 33):
+        X, _ = synthetic.dense_operands(M, 8, K, kind="prefill", seed=seed)
+        A8, sA = b.fp8_quant_1x128(dev(X))
+        outs.append(b.fp8gemm_dense(A8, sA, B8, sB))
+        xs.append(X)
+    for X, got in zip(xs, outs):
+        Ao, sAo = oquant.quant_1x128_fast(X)
+        assert_close(host(got), ogemm.gemm_dense(Ao, sAo, Bo, sBo), f"chained {M}x{N}x{K}")
     assert b.fp8gemm_get_device_status() == b.OK
 
 
