@@ -143,3 +143,42 @@ def test_masked_full_size_sampled():
         rows = np.unique(np.array([0, mm[e] - 1, mm[e] // 2, min(127, mm[e] - 1)]))
         ref = ogemm.gemm_dense_at(A[e], sA[e], B[e], sB[e], rows, cols)
         assert_close(got[e][rows][:, cols], ref, f"masked expert {e}")
+
+
+@pytest.mark.parametrize("form", ["masked", "contiguous"])
+def test_grouped_after_quantiser_without_host_sync(form):
+    """The grouped GEMMs are launched as programmatic dependents of the
+    previous kernel: quantise each batch's FP32 activations on the device and
+    run the GEMM right after, two batches back to back, no host sync."""
+    b = _b()
+    E, N, K = 6, 2048, 4096
+    outs, refs = [], []
+    for seed in (41, 42):
+        if form == "masked":
+            mm = np.array([256, 1, 130, 0, 64, 200], np.int32)
+            X, W, mm = synthetic.masked_operands(E, 256, N, K, seed=seed, masked_m=mm)
+            Xf = X.reshape(-1, K)
+        else:
+            X, W, lay = synthetic.contiguous_operands(E, 900, N, K, seed=seed)
+            Xf = X
+        Bq = [quant_weights(W[e]) for e in range(E)]
+        B = np.stack([q for q, _ in Bq])
+        sB = np.stack([s for _, s in Bq])
+        A8, sA = b.fp8_quant_1x128(dev(Xf))
+        Ao, sAo = oquant.quant_1x128_fast(Xf)
+        if form == "masked":
+            A8, sA = A8.view(E, 256, K), sA.view(E, 256, K // 128)
+            outs.append((b.fp8gemm_grouped_masked(A8, sA, dev(B), dev(sB), dev(mm)), mm))
+            refs.append(ogemm.gemm_masked(Ao.reshape(E, 256, K), sAo.reshape(E, 256, -1), B, sB, mm))
+        else:
+            mi = lay.m_indices.astype(np.int32)
+            outs.append((b.fp8gemm_grouped_contiguous(A8, sA, dev(B), dev(sB), dev(mi)), None))
+            refs.append(ogemm.gemm_contiguous(Ao, sAo, B, sB, mi))
+    for (got, mm), ref in zip(outs, refs):
+        got = host(got)
+        if mm is not None:  # rows past masked_m are not outputs
+            for e in range(E):
+                assert_close(got[e, :mm[e]], ref[e, :mm[e]], f"{form} expert {e}")
+        else:
+            assert_close(got, ref, form)
+    assert b.fp8gemm_get_device_status() == b.OK
