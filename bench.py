@@ -122,7 +122,9 @@ class ClockSampler:
         text = self.file.read()
         self.file.close()
         os.unlink(self.file.name)
-        return self.summarise(text, self.t0, self.t1)
+        out = self.summarise(text, self.t0, self.t1)
+        out["source"] = "nvidia-smi, 10 ms"
+        return out
 
     @classmethod
     def summarise(cls, text, t0=None, t1=None):
@@ -134,21 +136,91 @@ class ClockSampler:
             r = [x.strip() for x in line.split(",")]
             try:
                 ts = datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
-                rows.append((ts, float(r[2]), float(r[3]), r[6:10]))
+                rows.append((ts, float(r[2]), float(r[3]),
+                             [name for name, v in zip(cls.REASONS, r[6:10])
+                              if v.lower() == "active"]))
             except (ValueError, IndexError):
                 continue
-        inside = [x for x in rows if t0 is not None and t0 <= x[0] <= t1]
-        use = inside or rows
-        reasons = set()
-        for _, _, _, flags in use:
-            for name, v in zip(cls.REASONS, flags):
-                if v.lower() == "active":
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(x[1] for x in use) if use else None,
-                "sm_max_mhz": max(x[2] for x in use) if use else None,
-                "samples": len(inside), "samples_total": len(rows),
-                "window_ms": round((t1 - t0) * 1e3, 1) if t0 is not None else None,
-                "reasons": sorted(reasons)}
+        return summarise_clock_rows(rows, t0, t1)
+
+
+def summarise_clock_rows(rows, t0=None, t1=None):
+    """rows: (host epoch s, SM MHz, max SM MHz, [active reason names]).
+    Median SM clock, max clock and reasons of the rows in [t0, t1] (every row
+    when t0 is None or no row falls inside)."""
+    inside = [x for x in rows if t0 is not None and t0 <= x[0] <= t1]
+    use = inside or rows
+    reasons = set()
+    for _, _, _, names in use:
+        reasons.update(names)
+    return {"sm_mhz": statistics.median(x[1] for x in use) if use else None,
+            "sm_max_mhz": max(x[2] for x in use) if use else None,
+            "samples": len(inside), "samples_total": len(rows),
+            "window_ms": round((t1 - t0) * 1e3, 1) if t0 is not None else None,
+            "reasons": sorted(reasons)}
+
+
+class NvmlClockSampler:
+    """The same record read from NVML (the driver's management library,
+    read-only queries) by a host thread every millisecond, so that even a
+    timed interval of a few milliseconds holds several samples.  start()
+    returns False where the library cannot be loaded (the caller then uses
+    ClockSampler)."""
+    BITS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+            0x4: "sw_power_cap"}
+
+    def __init__(self, gpu_index, period_s=0.001):
+        self.gpu = gpu_index
+        self.period = period_s
+        self.rows = []
+        self.t0 = self.t1 = None
+        self._stop = None
+        self._thread = None
+
+    def start(self):
+        import ctypes
+        import threading
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return False
+            h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.gpu), ctypes.byref(h)) != 0:
+                return False
+            reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, ctypes.c_int(1), ctypes.byref(mx)) != 0:
+                return False
+        except (OSError, AttributeError):
+            return False
+        self._nv, self._h, self._reasons_fn, self._max = nv, h, reasons_fn, float(mx.value)
+        self._stop = threading.Event()
+        self._thread = threading.Thread(target=self._run, daemon=True)
+        self._thread.start()
+        return True
+
+    def _run(self):
+        import ctypes
+        clk, bits = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            t = time.time()
+            if (self._nv.nvmlDeviceGetClockInfo(self._h, ctypes.c_int(1), ctypes.byref(clk)) == 0 and
+                    self._reasons_fn(self._h, ctypes.byref(bits)) == 0):
+                names = [n for b, n in self.BITS.items() if bits.value & b]
+                self.rows.append((t, float(clk.value), self._max, names))
+            time.sleep(self.period)
+
+    def window(self, t0, t1):
+        self.t0, self.t1 = t0, t1
+
+    def stop(self):
+        self._stop.set()
+        self._thread.join(timeout=5)
+        self._nv.nvmlShutdown()
+        out = summarise_clock_rows(self.rows, self.t0, self.t1)
+        out["source"] = "nvml, 1 ms"
+        return out
 
 
 # ------------------------------------------------------------- GPU arm
@@ -233,8 +305,10 @@ def run_gpu(args, rank, world):
           for _ in range(K_steps)]
     gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(K_steps)]
-    clocks = ClockSampler(torch.cuda.current_device())
-    clocks.start()
+    clocks = NvmlClockSampler(torch.cuda.current_device())
+    if not clocks.start():
+        clocks = ClockSampler(torch.cuda.current_device())
+        clocks.start()
     time.sleep(0.3)
     launches0 = b.num_kernel_launches()
     if world > 1:

@@ -130,3 +130,20 @@ def test_end_to_end_gemm_parts_keep_whole_tile_waves():
         p = bench.gemm_parts(M, N, chunks, sms)
         assert chunks % p == 0
         assert p == 1 or (M // p) // 128 * -(-N // 256) >= sms
+
+
+def test_clock_rows_summary_and_nvml_fallback():
+    """The NVML sampler's rows go through the same window summary; where the
+    management library cannot be loaded (no driver here) it declines, and the
+    bench falls back to the nvidia-smi sampler."""
+    import bench
+    rows = [(1.0, 1500.0, 2070.0, []), (2.0, 2070.0, 2070.0, ["sw_power_cap"]),
+            (2.5, 2055.0, 2070.0, []), (3.0, 2070.0, 2070.0, []), (9.0, 990.0, 2070.0, ["hw_slowdown"])]
+    s = bench.summarise_clock_rows(rows, 1.9, 3.1)
+    assert s["samples"] == 3 and s["samples_total"] == 5
+    assert s["sm_mhz"] == 2070.0 and s["reasons"] == ["sw_power_cap"]
+    s = bench.summarise_clock_rows(rows)
+    assert s["samples"] == 0 and s["reasons"] == ["hw_slowdown", "sw_power_cap"]
+    import ctypes.util
+    if ctypes.util.find_library("nvidia-ml") is None:
+        assert bench.NvmlClockSampler(0).start() is False
