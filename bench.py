@@ -275,16 +275,28 @@ def run_gpu(args, rank, world):
     flush = L2Flush(dev)
     flops_step = sum(2.0 * c["M"] * c["N"] * c["K"] for c in cases)
 
-    def step(gemm_events=None):
+    batched = args.gemm_form == "batch"
+    batch = [(c["A8"], c["sA"], c["B8"], c["sB"], c["D"]) for c in cases]
+
+    def step(gemm_events=None, batched=batched):
         # both quantisers first: while they run, the host enqueues the GEMMs,
-        # so the device never waits on the host inside a step.  Then the
-        # other GEMMs, and last the dominant one (cases[0]) between the two
-        # events that time it: an event between two kernels ends the
-        # programmatic overlap of the second with the first, so only the
-        # dominant GEMM's start pays for it (its end is followed by the next
-        # step's L2 flush, not a programmatic launch)
+        # so the device never waits on the host inside a step.  Then the GEMMs:
+        # by default both shapes in one launch (fp8gemm_dense_batch: the
+        # short tiles of 4096^3 fill the last round of the long ones), timed
+        # between two events; with --gemm-form single, one call per shape,
+        # the dominant one (cases[0]) last and alone between the events: an
+        # event between two kernels ends the programmatic overlap of the
+        # second with the first, so only the timed GEMM's start pays for it
+        # (its end is followed by the next step's L2 flush)
         for c in cases:
             b.fp8_quant_1x128(c["X"], Q=c["A8"], sX=c["sA"])
+        if batched:
+            if gemm_events is not None:
+                gemm_events[0].record(stream)
+            b.fp8gemm_dense_batch(batch)
+            if gemm_events is not None:
+                gemm_events[1].record(stream)
+            return
         for c in cases[1:] + cases[:1]:
             timed = gemm_events is not None and c is cases[0]
             if timed:
@@ -332,27 +344,41 @@ def run_gpu(args, rank, world):
 
     step_ms = [s.elapsed_time(e) for s, e in ev]
     ms_per_step = sum(step_ms) / K_steps
-    gemm_ms = sum(g[0].elapsed_time(g[1]) for g in gev) / K_steps  # the dominant GEMM
+    gemm_ms = sum(g[0].elapsed_time(g[1]) for g in gev) / K_steps  # the timed GEMM launch
     ms_per_step = max_over_ranks(ms_per_step, world)
     value = aggregate_tflops(flops_step, ms_per_step, world)
 
-    # roofline of the dominant kernel: the dense GEMM on the 4096x7168x16384
-    # shape (about 70 % of the step)
-    gemm_flops = 2.0 * cases[0]["M"] * cases[0]["N"] * cases[0]["K"]
+    # roofline of the dominant kernel: the tensor-core GEMM launch -- both
+    # prefill shapes in one batched launch (about 85 % of the step), or with
+    # --gemm-form single the 4096x7168x16384 launch alone (about 70 %)
+    timed_shapes = PREFILL_SHAPES if batched else PREFILL_SHAPES[:1]
+    gemm_flops = sum(2.0 * M * N * K for M, N, K in timed_shapes)
     achieved = gemm_flops / (gemm_ms * 1e-3) / 1e12
     # each step is short (sub-ms) and starts after an L2 flush at full clock:
     # the burst figure is the denominator; the sustained one is listed beside
     peak = fp8_peak(peaks, sustained=False)
-    roofline = {"kernel": "gemm_tc_kernel<BN=256> (fp8gemm_dense, M > 64), M=4096 N=7168 K=16384",
+    kernel = ("gemm_tc_kernel<BN=256, batched> (fp8gemm_dense_batch): 4096x7168x16384 and "
+              "4096x4096x4096 in one launch" if batched else
+              "gemm_tc_kernel<BN=256> (fp8gemm_dense, M > 64), M=4096 N=7168 K=16384")
+    traffic_key = "gemm_tc_batch_prefill_pair" if batched else "gemm_tc_dense_4096x7168x16384"
+    roofline = {"kernel": kernel,
                 "bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1),
                 "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                 "peak_source": (f"{peaks['source']} bf16 burst x 2 (FP8/BF16 nominal ratio): "
                                 "the kernel is timed in sub-ms steps after an L2 flush"),
                 "frac_of_sustained_peak": round(achieved / fp8_peak(peaks, True), 4),
                 "measured_fp8_tflops": measure_library_fp8(*PREFILL_SHAPES[0], flush),
-                "traffic": traffic_from_profiles("gemm_tc_dense_4096x7168x16384"),
-                "algorithmic_bytes": gemm_bytes(*PREFILL_SHAPES[0]),
+                "traffic": traffic_from_profiles(traffic_key),
+                "algorithmic_bytes": sum(gemm_bytes(*shp) for shp in timed_shapes),
                 "gemm_us": round(1e3 * gemm_ms, 2)}
+
+    # ---- the other form of the step's GEMMs, whole steps only (no event
+    # between its kernels, so every programmatic overlap stays), and that
+    # form's GEMM launch(es) alone with L2 flushed
+    other = None
+    if not args.no_extras:
+        other = measure_other_form(step, not batched, batch, cases, flush, flops_step, peaks,
+                                   max(5, min(K_steps, 50)))
 
     # ---- end to end through the public API with host buffers
     e2e = measure_e2e(args, cases, flops_step, world)
@@ -376,7 +402,48 @@ def run_gpu(args, rank, world):
         del cases
         torch.cuda.empty_cache()
         out["configs"] = measure_configs(peaks, dev)
+        out["configs"][other["name"]] = other
     return out
+
+
+def measure_other_form(step, batched, batch, cases, flush, flops_step, peaks, n):
+    """The prefill step with the GEMM form the main measurement did not use:
+    mean time of n whole steps (L2 flushed before each, events around the
+    step only), and the GEMM launch(es) of that form timed alone."""
+    import torch
+
+    from fp8_fine_grained_e4m3_gb300 import binding as b
+    stream = torch.cuda.current_stream()
+    for i in range(3):
+        flush(i)
+        step(batched=batched)
+    ts = []
+    for i in range(n):
+        flush(i)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        step(batched=batched)
+        e.record(stream)
+        e.synchronize()
+        ts.append(s.elapsed_time(e))
+    ms = sum(ts) / n
+    if batched:
+        gemm = lambda: b.fp8gemm_dense_batch(batch)  # noqa: E731
+    else:
+        def gemm():
+            for c in cases:
+                b.fp8gemm_dense(c["A8"], c["sA"], c["B8"], c["sB"], D=c["D"])
+    g_ms = time_launch(gemm, flush)
+    g_tflops = flops_step / (g_ms * 1e-3) / 1e12
+    peak = fp8_peak(peaks, sustained=False)
+    return {"name": "prefill_step_batched_gemm" if batched else "prefill_step_single_gemms",
+            "ms_per_step": round(ms, 4), "tflops": round(flops_step / (ms * 1e-3) / 1e12, 1),
+            "gemm_us": round(1e3 * g_ms, 2), "gemm_tflops": round(g_tflops, 1),
+            "gemm_frac": round(g_tflops / peak, 4),
+            "form": ("both shapes in one fp8gemm_dense_batch launch" if batched else
+                     "one fp8gemm_dense call per shape"),
+            "timing": "whole steps (quantisers + GEMMs), L2 flushed before each; the GEMMs "
+                      "alone by time_launch"}
 
 
 def gemm_parts(M, N, chunks, sms):
@@ -872,7 +939,16 @@ def run_kernel_case(name, reps):
     shapes = {"gemm_prefill": (4096, 7168, 16384), "gemm_square": (4096, 4096, 4096),
               "gemm_decode64": (64, 7168, 2048), "gemm_decode1": (1, 7168, 2048),
               "gemm_split": (128, 4096, 7168), "quant": (4096, 8, 16384)}
-    if name in shapes:
+    if name == "gemm_prefill_batch":  # both prefill shapes in one batched launch
+        ops = []
+        for i, (M, N, K) in enumerate(PREFILL_SHAPES):
+            X, W = synthetic.dense_operands_device(M, N, K, kind="prefill", seed=i, device=dev)
+            A8, sA = b.fp8_quant_1x128(X)
+            B8, sB = b.fp8_quant_128x128(W)
+            del X, W
+            ops.append((A8, sA, B8, sB, torch.empty((M, N), dtype=torch.bfloat16, device=dev)))
+        fn = lambda: b.fp8gemm_dense_batch(ops)  # noqa: E731
+    elif name in shapes:
         M, N, K = shapes[name]
         X, W = synthetic.dense_operands_device(M, N, K, kind="prefill", seed=0, device=dev)
         A8, sA = b.fp8_quant_1x128(X)
@@ -940,6 +1016,9 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--gemm-form", choices=["single", "batch"], default="single",
+                    help="the step's GEMMs: one call per shape (the dominant one timed alone), "
+                         "or both shapes in one batched launch (timed as one kernel)")
     ap.add_argument("--no-extras", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)

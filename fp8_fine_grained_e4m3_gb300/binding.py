@@ -48,6 +48,7 @@ SIGNATURES = [
     ("fp8gemm_dense_fmt", _I, [_P, _P, _I, _P, _P, _I, _P, _I, _I, _I, _P]),
     ("fp8gemm_dense_ex", _I, [_P, _P, _I, _P, _P, _I, _P, _I, _I, _I, ctypes.c_uint, _P]),
     ("fp8gemm_grouped_table", _I, [_P, _I, _I, _P]),
+    ("fp8gemm_dense_batch", _I, [_P, _I, _P]),
     ("fp8gemm_grouped_contiguous_fmt", _I,
      [_P, _P, _I, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P]),
     ("fp8gemm_grouped_masked_fmt", _I, [_P, _P, _I, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P]),
@@ -423,6 +424,38 @@ def problem_table(problems, out=None):
         return host.to("cuda")
     out.copy_(host)
     return out
+
+
+MAX_DENSE_BATCH = 4  # FP8GEMM_MAX_DENSE_BATCH
+
+
+def fp8gemm_dense_batch(problems, stream=None):
+    """Independent dense problems in one launch: `problems` is a list of at
+    most MAX_DENSE_BATCH tuples (A, sA, B, sB) or (A, sA, B, sB, D), optionally
+    followed by (a_fmt, b_fmt); returns the list of D (bf16 [M, N], allocated
+    where not given).  The entries are read on the host during the call."""
+    torch = _torch()
+    if len(problems) > MAX_DENSE_BATCH:
+        raise ValueError(f"{len(problems)} problems; one call takes at most {MAX_DENSE_BATCH}")
+    arr = (Problem * max(len(problems), 1))()
+    outs = []
+    for e, prob in zip(arr, problems):
+        A, sA, B, sB = prob[:4]
+        D = prob[4] if len(prob) in (5, 7) else None
+        fmts = prob[-2:] if len(prob) in (6, 7) else ("e4m3", "e4m3")
+        A, B = _u8_fmt(A, fmts[0], "A"), _u8_fmt(B, fmts[1], "B")
+        M, N, K = _dense_mnk(A, B)
+        if D is None:
+            D = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+        _shape_dense(A, _f32(sA, "sA"), B, _f32(sB, "sB"), D, M, N, K)
+        e.A, e.sA, e.B = _ptr(A, "A").value, _ptr(sA, "sA").value, _ptr(B, "B").value
+        e.sB, e.D = _ptr(sB, "sB").value, _ptr(D, "D").value
+        e.M, e.N, e.K = M, N, K
+        e.formats = _fmt(fmts[0]) | (_fmt(fmts[1]) << 8)
+        outs.append(D)
+    _check(lib().fp8gemm_dense_batch(ctypes.cast(arr, _P), len(problems), _stream(stream)),
+           "fp8gemm_dense_batch")
+    return outs
 
 
 def fp8gemm_grouped_table(table, num_problems, max_M, stream=None):

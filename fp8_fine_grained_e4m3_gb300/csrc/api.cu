@@ -152,7 +152,8 @@ int finish(cudaError_t e, int nlaunch) {
 // activations of fp8gemm_dense_quant_a at large M -- a separate buffer, so
 // those bytes never land on the counters.
 // Slot kWsTable: the stream-K partials and counters of the problem-table GEMM.
-enum { kWsSplitK = 0, kWsQuantA = 1, kWsTable = 2 };
+// Slot kWsBatch: the tile counters of the batched dense GEMM.
+enum { kWsSplitK = 0, kWsQuantA = 1, kWsTable = 2, kWsBatch = 3 };
 
 int workspace_for(cudaStream_t s, size_t bytes, void** out, int slot = kWsSplitK) {
   int dev = 0;
@@ -409,6 +410,36 @@ int fp8gemm_grouped_table(const fp8gemm_problem* problems, int num_problems, int
 }
 
 static bool valid_fmt(int f) { return f == FP8GEMM_FMT_E4M3 || f == FP8GEMM_FMT_E5M2; }
+
+int fp8gemm_dense_batch(const fp8gemm_problem* problems, int num_problems,
+                        fp8gemm_stream_t stream) {
+  if (num_problems < 0 || num_problems > FP8GEMM_MAX_DENSE_BATCH) return FP8GEMM_ERR_SHAPE;
+  if (num_problems == 0) return FP8GEMM_OK;
+  if (!problems) return FP8GEMM_ERR_NULL;
+  bool any = false;
+  for (int i = 0; i < num_problems; ++i) {  // every entry is checked before anything runs
+    const fp8gemm_problem& q = problems[i];
+    if (int r = check_common(q.M, q.N, q.K)) return r;
+    if ((long long)q.M * q.K > (1LL << 46) || (long long)q.N * q.K > (1LL << 46))
+      return FP8GEMM_ERR_SHAPE;
+    if (!valid_fmt(q.formats & 0xff) || !valid_fmt(q.formats >> 8)) return FP8GEMM_ERR_FORMAT;
+    if (q.M == 0 || q.N == 0) continue;
+    if (!q.A || !q.sA || !q.B || !q.sB || !q.D) return FP8GEMM_ERR_NULL;
+    if (!aligned16(q.A) || !aligned16(q.sA) || !aligned16(q.B) || !aligned16(q.sB) ||
+        !aligned16(q.D))
+      return FP8GEMM_ERR_ALIGN;
+    any = true;
+  }
+  if (!any) return FP8GEMM_OK;
+  LaunchCtx c;
+  if (int r = ctx_for(stream, &c)) return r;
+  void* ws = nullptr;
+  if (int r = workspace_for(stream, 256, &ws, kWsBatch)) return r;
+  int launches = 0;
+  const cudaError_t e = launch_gemm_tc_batch(c, problems, num_problems,
+                                             static_cast<unsigned int*>(ws), &launches);
+  return finish(e, launches);
+}
 
 int fp8gemm_grouped_contiguous_fmt(const uint8_t* A, const float* sA, int a_fmt,
                                    const uint8_t* B, const float* sB, int b_fmt,

@@ -75,6 +75,11 @@ constexpr int kMaxSplit = 8;  // parts (cluster CTAs) per split tile, at most
 
 // The persistent tensor-core GEMM (one launch; the count goes to *launches).
 cudaError_t launch_gemm_tc(const LaunchCtx& c, const GemmArgs& a, int* launches);
+// Up to FP8GEMM_MAX_DENSE_BATCH independent dense problems (host array `p`,
+// validated) in one launch of the persistent tensor-core GEMM, tiles handed
+// out through `counter` (two zeroed words; each launch leaves them at zero).
+cudaError_t launch_gemm_tc_batch(const LaunchCtx& c, const fp8gemm_problem* p, int count,
+                                 unsigned int* counter, int* launches);
 cudaError_t launch_gemm_small_m(const LaunchCtx& c, const GemmArgs& a, void* workspace,
                                 size_t workspace_bytes);
 size_t small_m_workspace_bytes(int num_sms, int N);

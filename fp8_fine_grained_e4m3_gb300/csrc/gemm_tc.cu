@@ -90,7 +90,9 @@ struct TcCfg {
   static_assert(kSmemBytes <= 232448, "227 KB of shared memory per CTA");
   static_assert(BN == 128 || BN == 256, "BN");
   static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM columns must be a power of 2");
-  static_assert((2 * kStages + 2 * kTmemBufs + 1) * 8 + 8 <= kBarBytes, "barrier area");
+  // full/empty per stage, TMEM full/empty, drain, TMEM address + abort flag,
+  // and (batched launches) the tile ring: 2 + 2 barriers and 2 slots of 32 B
+  static_assert((2 * kStages + 2 * kTmemBufs + 6) * 8 + 64 <= kBarBytes, "barrier area");
 };
 
 struct Tile {
@@ -99,7 +101,68 @@ struct Tile {
   int n0;          // first output column
   int b_row0;      // first row in B's 2-D row space (expert * N + n0)
   int e;           // expert (0 for dense)
+  int p;           // problem of a batched launch (0 otherwise)
+  int kb;          // K blocks of that problem (batched launch only)
 };
+
+// A batched launch (fp8gemm_dense_batch): independent dense problems, each
+// with its own tensor maps and sizes, whose tiles form one sequence -- the
+// problems one after another, each in the grouped rasterisation order of the
+// dense form.  The persistent CTAs take their first tile by index and every
+// later one from a counter (the next unclaimed tile when a CTA's producer
+// has issued its current tile's loads), so CTAs that finish early take more
+// tiles: with the problems ordered by falling K, the short tiles of the last
+// problems fill the partial last round of the long ones.  The producer hands
+// each tile index to the MMA and promotion warps through a two-slot ring in
+// shared memory; each role maps the index to its tile itself (handing over
+// the mapped fields instead cost the promotion warps a register spill and
+// 7 % on 4096x7168x16384).
+constexpr int kMaxBatch = FP8GEMM_MAX_DENSE_BATCH;
+
+struct BatchProblem {
+  const float* sA;
+  const float* sB;
+  __nv_bfloat16* D;
+  int M, N, Kb;
+  int num_m, num_n;
+  int tile0;  // its first tile in the launch's sequence
+  int fmts;   // a_fmt | b_fmt << 8
+  int d_tma;  // the D map is valid
+};
+
+template <int P>
+struct BatchParams {
+  CUtensorMap a[P], b[P], d[P];
+  BatchProblem prob[P];
+  int count;              // problems in use (the rest are never read)
+  int total;              // tiles of all problems
+  unsigned int* counter;  // [0] tiles claimed past the first round, [1] CTAs done
+};
+template <>
+struct BatchParams<0> {};  // the single-problem instances
+
+// Tile t of a batched launch (t < total).
+template <int P>
+__device__ __forceinline__ void batch_tile(const BatchParams<P>& bp, int t, int BN, Tile& tile) {
+  int p = 0;
+#pragma unroll
+  for (int q = 1; q < P; ++q)
+    if (q < bp.count && t >= bp.prob[q].tile0) p = q;
+  const BatchProblem& pr = bp.prob[p];
+  t -= pr.tile0;
+  const int per_group = kGroupM * pr.num_n;
+  const int g = t / per_group;
+  const int first_m = g * kGroupM;
+  const int gs = min(kGroupM, pr.num_m - first_m);
+  const int r = t - g * per_group;
+  tile.row0 = (first_m + r % gs) * kBlockM;
+  tile.n0 = (r / gs) * BN;
+  tile.b_row0 = tile.n0;
+  tile.e = 0;
+  tile.valid_rows = min(kBlockM, pr.M - tile.row0);
+  tile.p = p;
+  tile.kb = pr.Kb;
+}
 
 // Walks the same tile sequence in every role of every CTA.
 struct Scheduler {
@@ -204,14 +267,19 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 
 // kSplit = false: whole tiles, persistent over the CTAs.  kSplit = true (all
 // tiles fit in one wave): cluster c of args.split CTAs computes tile c, CTA
-// rank r the r-th share of its K blocks.
-template <class Cfg, bool kSplit>
+// rank r the r-th share of its K blocks.  kP > 0: a batched launch of up to
+// kP dense problems (whole tiles; maps, sizes and pointers from `bp`, the
+// first three parameters and args' problem fields unused).
+template <class Cfg, bool kSplit, int kP = 0>
 __global__ void __launch_bounds__(Cfg::kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmD, const GemmArgs args, int* status) {
+                   const __grid_constant__ CUtensorMap tmD, const GemmArgs args, int* status,
+                   const __grid_constant__ BatchParams<kP> bp) {
   constexpr int BN = Cfg::BN;
   constexpr int kStages = Cfg::kStages;
+  constexpr bool kBatch = kP > 0;
+  static_assert(!(kBatch && kSplit), "batched launches take whole tiles");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -228,6 +296,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   uint64_t* drain_bar = bars + 2 * kStages + 2 * NB;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 2 * NB + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  // batched launches: the tile ring (slot: a tile index, -1 ends the
+  // sequence; 32-byte slots)
+  uint64_t* ring_full = bars + 2 * kStages + 2 * NB + 2;
+  uint64_t* ring_empty = ring_full + 2;
+  int* ring = reinterpret_cast<int*>(ring_full + 4);
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -242,6 +315,12 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       mbar_init(&tempty_bar[b], Cfg::kPromoWarps);
     }
     mbar_init(drain_bar, 1);
+    if constexpr (kBatch) {
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&ring_full[i], 1);                       // the producer
+        mbar_init(&ring_empty[i], 1 + Cfg::kPromoWarps);  // MMA thread + promotion warps
+      }
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -250,9 +329,17 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     tmem_relinquish();
   }
   if (warp == Cfg::kTmaWarp && lane == 0) {
-    tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
-    if (args.d_tma) tma_prefetch_desc(&tmD);
+    if constexpr (kBatch) {
+      for (int q = 0; q < bp.count; ++q) {
+        tma_prefetch_desc(&bp.a[q]);
+        tma_prefetch_desc(&bp.b[q]);
+        if (bp.prob[q].d_tma) tma_prefetch_desc(&bp.d[q]);
+      }
+    } else {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+      if (args.d_tma) tma_prefetch_desc(&tmD);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -287,6 +374,25 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     *abort_flag = 1;
     raise_status(status, FP8GEMM_ERR_TIMEOUT);
   };
+  // Batched launches: the next tile index from the ring (-1 at the end of
+  // the sequence or when the wait gave up).  A promotion warp calls it with
+  // all lanes (whole_warp: they agree on the outcome, and every lane has read
+  // the slot before it is released); the MMA thread alone.
+  uint32_t ring_taken = 0;
+  auto ring_index = [&](bool whole_warp) -> int {
+    const int slot = int(ring_taken & 1);
+    bool got = mbar_wait(&ring_full[slot], (ring_taken >> 1) & 1, abort_flag, args.wait_ns);
+    if (whole_warp) got = __all_sync(0xffffffffu, got);
+    if (!got) {
+      fail();
+      return -1;
+    }
+    const int t = ring[slot * 8];
+    if (whole_warp) __syncwarp();
+    if (lane == 0) mbar_arrive(&ring_empty[slot]);
+    ++ring_taken;
+    return t;
+  };
 
   // Register budgets change at the top of each role (setmaxnreg, per
   // warpgroup): the producer warpgroup gives registers to the promotion ones.
@@ -296,7 +402,44 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      for (int t = first_tile(t_begin); t < end_tile(t_end) && ok; t += tile_step()) {
+      if constexpr (kBatch) {
+        // first tile by index, then each from the counter once the current
+        // tile's loads are issued; every tile is published on the ring, then
+        // the end marker
+        uint32_t published = 0;
+        int t = int(blockIdx.x);
+        while (ok) {
+          Tile tile;
+          const bool have = t < bp.total;
+          if (have) batch_tile(bp, t, BN, tile);
+          const int slot = int(published & 1);
+          if (!mbar_wait(&ring_empty[slot], ((published >> 1) & 1) ^ 1, abort_flag,
+                         args.wait_ns)) {
+            fail();
+            break;
+          }
+          ring[slot * 8] = have ? t : -1;
+          mbar_arrive(&ring_full[slot]);
+          ++published;
+          if (!have) break;
+          const CUtensorMap* mA = &bp.a[tile.p];
+          const CUtensorMap* mB = &bp.b[tile.p];
+          for (int kb = 0; kb < tile.kb; ++kb, ++it) {
+            const int s = it % kStages;
+            const uint32_t ph = (it / kStages) & 1;
+            if (!mbar_wait(&empty_bar[s], ph ^ 1, abort_flag, args.wait_ns)) {
+              fail();
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&full_bar[s], Cfg::kStageBytes);
+            tma_load_2d(smA + s * Cfg::kABytes, mA, &full_bar[s], kb * kBlockK, tile.row0);
+            tma_load_2d(smB + s * Cfg::kBBytes, mB, &full_bar[s], kb * kBlockK, tile.b_row0);
+          }
+          if (ok) t = int(gridDim.x) + int(atomicAdd(bp.counter, 1u));
+        }
+      }
+      for (int t = first_tile(t_begin); !kBatch && t < end_tile(t_end) && ok; t += tile_step()) {
         Tile tile;
         if (!sched.get(t, BN, tile)) continue;
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
@@ -326,10 +469,21 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       const uint32_t b_base = smem_addr(smB);
       uint32_t it = 0;
       bool ok = true;
-      for (int t = first_tile(t_begin); t < end_tile(t_end) && ok; t += tile_step()) {
+      for (int t = kBatch ? ring_index(false) : first_tile(t_begin);
+           (kBatch ? t >= 0 : t < end_tile(t_end)) && ok;
+           t = kBatch ? ring_index(false) : t + tile_step()) {
         Tile tile;
-        if (!sched.get(t, BN, tile)) continue;
-        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+        uint32_t idesc_t = idesc;
+        int kb_end = kb1;
+        if constexpr (kBatch) {
+          batch_tile(bp, t, BN, tile);
+          const int f = bp.prob[tile.p].fmts;
+          idesc_t = idesc_f8_f32(kBlockM, BN, uint32_t(f & 0xff), uint32_t(f >> 8));
+          kb_end = tile.kb;
+        } else if (!sched.get(t, BN, tile)) {
+          continue;
+        }
+        for (int kb = kb0; kb < kb_end; ++kb, ++it) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1;
           const int buf = it % NB;
@@ -346,7 +500,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           for (int k = 0; k < kBlockK / 32; ++k) {
             const uint64_t ad = smem_desc_sw128_kmajor(a_base + s * Cfg::kABytes + k * 32);
             const uint64_t bd = smem_desc_sw128_kmajor(b_base + s * Cfg::kBBytes + k * 32);
-            umma_e4m3(d_tmem, ad, bd, idesc, k > 0 ? 1u : 0u);
+            umma_e4m3(d_tmem, ad, bd, idesc_t, k > 0 ? 1u : 0u);
           }
           umma_commit(&empty_bar[s]);     // stage free once these MMAs finish
           umma_commit(&tfull_bar[buf]);   // partial ready for promotion
@@ -367,14 +521,32 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     uint32_t it = 0;
     uint32_t n_stores = 0;  // TMA stores this warp has issued (alternates the boxes)
     bool ok = true;
-    for (int t = first_tile(t_begin); t < end_tile(t_end) && ok; t += tile_step()) {
+    for (int t = kBatch ? ring_index(true) : first_tile(t_begin);
+         (kBatch ? t >= 0 : t < end_tile(t_end)) && ok;
+         t = kBatch ? ring_index(true) : t + tile_step()) {
       Tile tile;
-      if (!sched.get(t, BN, tile)) continue;
+      if constexpr (kBatch) {
+        batch_tile(bp, t, BN, tile);
+      } else if (!sched.get(t, BN, tile)) {
+        continue;
+      }
       const bool row_ok = row < tile.valid_rows;
       const int col0 = tile.n0 + wg * Cfg::kColsPerWG;  // first column of this warpgroup
-      const bool cols_ok = col0 < args.N;
-      const float* sa_ptr = args.sA + size_t(tile.row0 + row) * Kb;
-      const float* sb_ptr = args.sB + (size_t(tile.e) * Nb + col0 / kBlockK) * Kb;
+      const float* sa_ptr;
+      const float* sb_ptr;
+      bool cols_ok;
+      int kb_end = kb1;
+      if constexpr (kBatch) {
+        const BatchProblem& pr = bp.prob[tile.p];
+        cols_ok = col0 < pr.N;
+        sa_ptr = pr.sA + size_t(tile.row0 + row) * tile.kb;
+        sb_ptr = pr.sB + size_t(col0 / kBlockK) * tile.kb;
+        kb_end = tile.kb;
+      } else {
+        cols_ok = col0 < args.N;
+        sa_ptr = args.sA + size_t(tile.row0 + row) * Kb;
+        sb_ptr = args.sB + (size_t(tile.e) * Nb + col0 / kBlockK) * Kb;
+      }
 
       // FP32 accumulator, two columns per float2 so the promotion runs on the
       // packed FMA (FFMA2)
@@ -384,9 +556,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 
       float sa_next = row_ok ? __ldg(sa_ptr + kb0) : 0.f;
       float sb_next = cols_ok ? __ldg(sb_ptr + kb0) : 0.f;
-      for (int kb = kb0; kb < kb1; ++kb, ++it) {
+      for (int kb = kb0; kb < kb_end; ++kb, ++it) {
         const float sc = sa_next * sb_next;
-        if (kb + 1 < kb1) {
+        if (kb + 1 < kb_end) {
           sa_next = row_ok ? __ldg(sa_ptr + kb + 1) : 0.f;
           sb_next = cols_ok ? __ldg(sb_ptr + kb + 1) : 0.f;
         }
@@ -442,11 +614,27 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       // store directly: 16 bytes at a time when rows of D are 16-byte
       // aligned (N % 8 == 0), else element by element.
       const int wrow0 = (warp % 4) * 32;  // first tile row of this warp
-      if (args.d_tma && wrow0 + 32 <= tile.valid_rows) {
+      int dN;
+      __nv_bfloat16* dD;
+      bool d_tma;
+      const CUtensorMap* mD;
+      if constexpr (kBatch) {
+        const BatchProblem& pr = bp.prob[tile.p];
+        dN = pr.N;
+        dD = pr.D;
+        d_tma = pr.d_tma != 0;
+        mD = &bp.d[tile.p];
+      } else {
+        dN = args.N;
+        dD = args.D;
+        d_tma = args.d_tma != 0;
+        mD = &tmD;
+      }
+      if (d_tma && wrow0 + 32 <= tile.valid_rows) {
         uint8_t* wbox = epi + warp * (2 * Cfg::kEpiBoxBytes);
 #pragma unroll
         for (int c = 0; c < Cfg::kColsPerWG / 32; ++c) {
-          if (col0 + 32 * c >= args.N) break;  // warp-uniform
+          if (col0 + 32 * c >= dN) break;  // warp-uniform
           uint8_t* box = wbox + (n_stores & 1) * Cfg::kEpiBoxBytes;
           // at most one store pending: the one before it, which used this
           // box, has finished reading it
@@ -469,24 +657,24 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&tmD, box, col0 + 32 * c, tile.row0 + wrow0);
+            tma_store_2d(mD, box, col0 + 32 * c, tile.row0 + wrow0);
             bulk_commit_group();
           }
           ++n_stores;
         }
-      } else if (row_ok && args.N % 8 != 0) {
-        __nv_bfloat16* drow = args.D + size_t(tile.row0 + row) * args.N + col0;
+      } else if (row_ok && dN % 8 != 0) {
+        __nv_bfloat16* drow = dD + size_t(tile.row0 + row) * dN + col0;
 #pragma unroll
         for (int j = 0; j < Cfg::kColsPerWG / 2; ++j) {
           const __nv_bfloat162 p = __float22bfloat162_rn(acc[j]);
-          if (col0 + 2 * j < args.N) drow[2 * j] = p.x;
-          if (col0 + 2 * j + 1 < args.N) drow[2 * j + 1] = p.y;
+          if (col0 + 2 * j < dN) drow[2 * j] = p.x;
+          if (col0 + 2 * j + 1 < dN) drow[2 * j + 1] = p.y;
         }
       } else if (row_ok) {
-        __nv_bfloat16* drow = args.D + size_t(tile.row0 + row) * args.N + col0;
+        __nv_bfloat16* drow = dD + size_t(tile.row0 + row) * dN + col0;
 #pragma unroll
         for (int j = 0; j < Cfg::kColsPerWG; j += 8) {
-          if (col0 + j < args.N) {
+          if (col0 + j < dN) {
             uint4 v;
             __nv_bfloat162 p0 = __float22bfloat162_rn(acc[j / 2 + 0]);
             __nv_bfloat162 p1 = __float22bfloat162_rn(acc[j / 2 + 1]);
@@ -554,13 +742,25 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   }
 
   __syncthreads();
+  if constexpr (kBatch) {
+    // every claim of this CTA precedes its count; the last CTA to count
+    // leaves both counters at zero for the next launch (which reads them
+    // only after this grid has completed)
+    if (threadIdx.x == 0) {
+      __threadfence();
+      if (atomicAdd(bp.counter + 1, 1u) == gridDim.x - 1) {
+        atomicExch(bp.counter, 0u);
+        atomicExch(bp.counter + 1, 0u);
+      }
+    }
+  }
   if (warp == Cfg::kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem_base, Cfg::kTmemCols);
   }
 }
 
-template <class Cfg, bool kSplit>
+template <class Cfg, bool kSplit, int kP = 0>
 cudaError_t set_smem_attr() {
   // once per device and context: the attribute belongs to the function in
   // one context, and a cudaDeviceReset gives the device a new one
@@ -569,7 +769,7 @@ cudaError_t set_smem_attr() {
   if (cudaError_t e = cudaGetDevice(&dev)) return e;
   const unsigned long long ctx = current_context_id();
   if (ctx != 0 && set_in[dev & 63] == ctx) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<Cfg, kSplit>,
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<Cfg, kSplit, kP>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        int(Cfg::kSmemBytes));
   if (e == cudaSuccess) set_in[dev & 63] = ctx;
@@ -667,7 +867,7 @@ cudaError_t run(const LaunchCtx& c, GemmArgs a, int* launches) {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     if (cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<Cfg, false>, tmA, tmB, tmD, a,
-                                           c.status))
+                                           c.status, BatchParams<0>{}))
       return e;
   } else {
     // one cluster per tile, as a programmatic dependent (its prologue
@@ -687,7 +887,7 @@ cudaError_t run(const LaunchCtx& c, GemmArgs a, int* launches) {
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     if (cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<Cfg, true>, tmA, tmB, tmD, a,
-                                           c.status))
+                                           c.status, BatchParams<0>{}))
       return e;
   }
   *launches = 1;
@@ -700,6 +900,74 @@ cudaError_t launch_gemm_tc(const LaunchCtx& c, const GemmArgs& a, int* launches)
   const bool wide = (a.N % 256 == 0) || a.N >= 2048;
   if (wide) return run<TcCfg<256, 4>>(c, a, launches);
   return run<TcCfg<128, 6>>(c, a, launches);
+}
+
+cudaError_t launch_gemm_tc_batch(const LaunchCtx& c, const fp8gemm_problem* p, int count,
+                                 unsigned int* counter, int* launches) {
+  using Cfg = TcCfg<256, 4>;
+  *launches = 0;
+  if (count < 0 || count > kMaxBatch) return cudaErrorInvalidValue;
+  // problems with work, longest K first (stable): the long tiles start in the
+  // first rounds and the short ones fill the end
+  int order[kMaxBatch];
+  int n = 0;
+  for (int i = 0; i < count; ++i) {
+    if (p[i].M <= 0 || p[i].N <= 0) continue;
+    int j = n++;
+    for (; j > 0 && ceil_div(p[order[j - 1]].K, kBlockK) < ceil_div(p[i].K, kBlockK); --j)
+      order[j] = order[j - 1];
+    order[j] = i;
+  }
+  if (n == 0) return cudaSuccess;
+  BatchParams<kMaxBatch> bp;
+  memset(&bp, 0, sizeof(bp));
+  long long total = 0;
+  for (int j = 0; j < n; ++j) {
+    const fp8gemm_problem& q = p[order[j]];
+    if (!make_tmap_u8_sw128(&bp.a[j], q.A, uint64_t(q.M), uint64_t(q.K), kBlockM))
+      return cudaErrorInvalidValue;
+    if (!make_tmap_u8_sw128(&bp.b[j], q.B, uint64_t(q.N), uint64_t(q.K), Cfg::BN))
+      return cudaErrorInvalidValue;
+    BatchProblem& pr = bp.prob[j];
+    pr.d_tma = make_tmap_bf16_sw64(&bp.d[j], q.D, uint64_t(q.M), uint64_t(q.N), 32) ? 1 : 0;
+    pr.sA = q.sA;
+    pr.sB = q.sB;
+    pr.D = static_cast<__nv_bfloat16*>(q.D);
+    pr.M = q.M;
+    pr.N = q.N;
+    pr.Kb = ceil_div(q.K, kBlockK);
+    pr.num_m = ceil_div(q.M, kBlockM);
+    pr.num_n = ceil_div(q.N, Cfg::BN);
+    pr.tile0 = int(total);
+    pr.fmts = q.formats;
+    total += (long long)pr.num_m * pr.num_n;
+    if (total > 0x7fffffffLL - 4LL * c.num_sms) return cudaErrorInvalidValue;
+  }
+  bp.count = n;
+  bp.total = int(total);
+  bp.counter = counter;
+  GemmArgs a{GemmMode::kDense, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, 0, 0, 0, 1};
+  a.wait_ns = wait_limit_ns();
+  CUtensorMap unused;
+  memset(&unused, 0, sizeof(unused));
+  if (cudaError_t e = set_smem_attr<Cfg, false, kMaxBatch>()) return e;
+  // persistent, one CTA per SM, as a programmatic dependent (see run())
+  const int grid = int(total < c.num_sms ? total : c.num_sms);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(grid));
+  cfg.blockDim = dim3(Cfg::kThreads);
+  cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+  cfg.stream = c.stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  if (cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<Cfg, false, kMaxBatch>, unused,
+                                         unused, unused, a, c.status, bp))
+    return e;
+  *launches = 1;
+  return cudaSuccess;
 }
 
 }  // namespace fp8gemm

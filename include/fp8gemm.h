@@ -351,6 +351,42 @@ int fp8gemm_grouped_table(const fp8gemm_problem* problems, int num_problems, int
                           fp8gemm_stream_t stream);
 
 /*
+ * fp8gemm_dense_batch -- up to FP8GEMM_MAX_DENSE_BATCH independent dense
+ * problems of prefill size in ONE launch of the 128-row tensor-core GEMM (the
+ * grouped GEMM of "bhfrc.com/news/60211" sections 4.2-4.3: one launch over a
+ * list of problems, each with its own M, N, K; here the list is on the host
+ * and fixed at the call).  Each problem's output tiles are those
+ * fp8gemm_dense computes for it on its whole-tile path; the persistent CTAs
+ * take the tiles of all problems from one shared sequence -- the problems
+ * with the longest K first, then each CTA its next tile when it finishes the
+ * last -- so the partial last round of one problem is filled with tiles of
+ * the next instead of leaving SMs idle.  A tile's arithmetic and summation
+ * order do not depend on which CTA takes it, so results are deterministic,
+ * and bit-identical to fp8gemm_dense_fmt's where that call takes its
+ * whole-tile path with 256-column tiles (N % 256 == 0 or N >= 2048, and at
+ * least as many tiles as SMs).
+ *
+ *   problems      HOST array of num_problems entries (read during the call;
+ *                 the library keeps no reference), layouts and rules per
+ *                 entry as for fp8gemm_grouped_table's entries, except that
+ *                 M has no upper bound and sA, sB and D are 16-byte aligned
+ *   num_problems  0..FP8GEMM_MAX_DENSE_BATCH
+ * The tiles are handed out through two counters in a per-(device, stream)
+ * workspace of 256 bytes that the library allocates and zeroes on the first
+ * such call on the stream (not during stream capture, see the conventions
+ * above); every launch leaves them at zero, so the call may be captured in a
+ * graph once the workspace exists.  Two launches of this call on one stream
+ * run in stream order and never share the counters at the same time.
+ * Entries with M = 0 or N = 0 are skipped.  Host-side errors:
+ * FP8GEMM_ERR_SHAPE (num_problems out of range, or an entry with a negative
+ * size, K = 0 or K % 16 != 0), FP8GEMM_ERR_FORMAT, FP8GEMM_ERR_NULL,
+ * FP8GEMM_ERR_ALIGN; nothing is enqueued then.
+ */
+#define FP8GEMM_MAX_DENSE_BATCH 4
+int fp8gemm_dense_batch(const fp8gemm_problem* problems, int num_problems,
+                        fp8gemm_stream_t stream);
+
+/*
  * fp8gemm_dense_small_m_noalloc -- the same computation as fp8gemm_dense for
  * decode-sized M (1..64), for callers that must not have the library allocate
  * device memory: a server that reserves its whole memory budget up front and

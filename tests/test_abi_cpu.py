@@ -119,3 +119,50 @@ def test_problem_struct_layout():
     body = hdr[hdr.index("typedef struct fp8gemm_problem"):hdr.index("} fp8gemm_problem;")]
     assert re.findall(r"\*\s*(\w+);", body) == ["A", "sA", "B", "sB", "D"]
     assert "int M, N, K;" in body and "int formats;" in body
+
+
+def test_dense_batch_host_validation_needs_no_gpu(lib):
+    """fp8gemm_dense_batch checks the count and every entry (sizes, formats,
+    pointers, alignment) before any CUDA call."""
+    from fp8_fine_grained_e4m3_gb300 import binding as b
+    P = ctypes.c_void_p
+    s = P(0)
+    good = 1 << 20
+
+    def entries(*rows):
+        arr = (b.Problem * len(rows))()
+        for e, (M, N, K, fmts, ptrs) in zip(arr, rows):
+            e.A, e.sA, e.B, e.sB, e.D = ptrs
+            e.M, e.N, e.K, e.formats = M, N, K, fmts
+        return ctypes.cast(arr, P), len(rows)
+
+    hdr = open(os.path.join(ROOT, "include", "fp8gemm.h")).read()
+    assert re.search(r"#define FP8GEMM_MAX_DENSE_BATCH (\d+)", hdr).group(1) == \
+        str(b.MAX_DENSE_BATCH)
+    ok5 = (good,) * 5
+    assert lib.fp8gemm_dense_batch(None, 0, s) == b.OK
+    assert lib.fp8gemm_dense_batch(None, -1, s) == b.ERR_SHAPE
+    assert lib.fp8gemm_dense_batch(None, b.MAX_DENSE_BATCH + 1, s) == b.ERR_SHAPE
+    assert lib.fp8gemm_dense_batch(None, 1, s) == b.ERR_NULL
+    # the second entry is bad: nothing is launched for the first either
+    assert lib.fp8gemm_dense_batch(*entries((256, 256, 256, 0, ok5), (128, 256, 200, 0, ok5)), s) \
+        == b.ERR_SHAPE
+    assert lib.fp8gemm_dense_batch(*entries((256, 256, 0, 0, ok5)), s) == b.ERR_SHAPE
+    assert lib.fp8gemm_dense_batch(*entries((256, -2, 256, 0, ok5)), s) == b.ERR_SHAPE
+    assert lib.fp8gemm_dense_batch(*entries((256, 256, 256, 2, ok5)), s) == b.ERR_FORMAT
+    assert lib.fp8gemm_dense_batch(*entries((256, 256, 256, 1 | (3 << 8), ok5)), s) == b.ERR_FORMAT
+    assert lib.fp8gemm_dense_batch(*entries((256, 256, 256, 0, (good, None, good, good, good))),
+                                   s) == b.ERR_NULL
+    assert lib.fp8gemm_dense_batch(*entries((256, 256, 256, 0, (good, good, good, good + 8, good))),
+                                   s) == b.ERR_ALIGN
+    # empty entries are skipped (no pointer needed): nothing to launch
+    assert lib.fp8gemm_dense_batch(*entries((0, 256, 256, 0, (None,) * 5),
+                                            (256, 0, 128, 1 | (1 << 8), (None,) * 5)), s) == b.OK
+
+
+def test_dense_batch_binding_refuses_on_host():
+    """The binding refuses more entries than one launch takes, before any
+    tensor is touched."""
+    from fp8_fine_grained_e4m3_gb300 import binding as b
+    with pytest.raises(ValueError, match="at most"):
+        b.fp8gemm_dense_batch([None] * (b.MAX_DENSE_BATCH + 1))
