@@ -281,10 +281,10 @@ def run_gpu(args, rank, world):
     def step(gemm_events=None, batched=batched):
         # both quantisers first: while they run, the host enqueues the GEMMs,
         # so the device never waits on the host inside a step.  Then the GEMMs:
-        # by default both shapes in one launch (fp8gemm_dense_batch: the
-        # short tiles of 4096^3 fill the last round of the long ones); with
-        # --gemm-form single, one call per shape, the dominant one (cases[0])
-        # last.  gemm_events (the roofline pass only) bracket the batched
+        # by default one call per shape, the dominant one (cases[0]) last;
+        # with --gemm-form batch, both shapes in one launch
+        # (fp8gemm_dense_batch: the short tiles of 4096^3 fill the last round
+        # of the long ones).  gemm_events (the roofline pass only) bracket the batched
         # launch, or the dominant single call: an event between two kernels
         # ends the programmatic overlap of the second with the first, which
         # is why the steps that give ms_per_step carry no such events
@@ -360,9 +360,9 @@ def run_gpu(args, rank, world):
     ms_per_step = max_over_ranks(ms_per_step, world)
     value = aggregate_tflops(flops_step, ms_per_step, world)
 
-    # roofline of the dominant kernel: the tensor-core GEMM launch -- both
-    # prefill shapes in one batched launch (about 85 % of the step), or with
-    # --gemm-form single the 4096x7168x16384 launch alone (about 70 %)
+    # roofline of the dominant kernel: the tensor-core GEMM launch -- the
+    # 4096x7168x16384 call (about 70 % of the step), or with --gemm-form
+    # batch the launch that runs both prefill shapes (about 85 %)
     timed_shapes = PREFILL_SHAPES if batched else PREFILL_SHAPES[:1]
     gemm_flops = sum(2.0 * M * N * K for M, N, K in timed_shapes)
     achieved = gemm_flops / (gemm_ms * 1e-3) / 1e12
@@ -1033,7 +1033,7 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    ap.add_argument("--gemm-form", choices=["batch", "single"], default="batch",
+    ap.add_argument("--gemm-form", choices=["single", "batch"], default="single",
                     help="the step's GEMMs: both shapes in one batched launch (the roofline "
                          "kernel), or one call per shape (the 4096x7168x16384 call the roofline "
                          "kernel)")
