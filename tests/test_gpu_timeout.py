@@ -37,3 +37,30 @@ def test_wait_timeout_is_reported_and_the_context_stays_usable():
     assert_close(host(b.fp8gemm_dense(*ops)), ref, "dense after the timeout")
     assert_close(host(b.fp8gemm_dense(*dops)), dref, "decode after the timeout")
     assert b.fp8gemm_get_device_status() == b.OK
+
+
+def test_batched_launch_timeout_leaves_the_next_launch_correct():
+    """The batched launch's extra waits (its tile ring) are bounded too: at a
+    1 ns limit the launch gives up with FP8GEMM_ERR_TIMEOUT, every CTA still
+    exits, and the next batched launches (on fresh counters: the timeout read
+    drops the workspaces) match the oracle."""
+    from fp8_fine_grained_e4m3_gb300 import binding as b
+    shapes = [(2048, 2560, 1024), (640, 768, 512)]
+    probs = [quantised_dense(M, N, K, "normal", seed=50 + i) for i, (M, N, K) in enumerate(shapes)]
+    ops = [tuple(dev(x) for x in p) for p in probs]
+    refs = [ogemm.gemm_dense(*p) for p in probs]
+    for D, r in zip(b.fp8gemm_dense_batch(ops), refs):  # the stream's counters exist
+        assert_close(host(D), r, "batch before")
+    assert b.fp8gemm_get_device_status() == b.OK
+    try:
+        b.set_wait_limit_ns(1)
+        b.fp8gemm_dense_batch(ops)
+        status = b.fp8gemm_get_device_status()
+    finally:
+        b.set_wait_limit_ns(0)
+    assert status == b.ERR_TIMEOUT, b.strerror(status)
+    assert b.workspace_bytes() == 0
+    for _ in range(2):
+        for D, r in zip(b.fp8gemm_dense_batch(ops), refs):
+            assert_close(host(D), r, "batch after the timeout")
+    assert b.fp8gemm_get_device_status() == b.OK
