@@ -10,7 +10,11 @@ Inputs are synthetic (A ~ N(0,1) with 1 % outlier columns x50, B ~ N(0,0.02)),
 drawn and kept on the device; L2 is flushed before every timed step (a
 256 MB write, then a 256 MB read so that no dirty line of the flush is
 written back inside the timed interval); each step is timed with CUDA events
-on the launching stream.
+on the launching stream, with no event between its kernels (an event there
+would end a kernel's programmatic overlap with the one before it); the
+roofline kernel is timed in a second pass of the same steps.  With
+`--gemm-form batch` the two GEMMs run as one fp8gemm_dense_batch launch; the
+form not chosen is timed as whole steps under `configs`.
 
 Printed: one JSON line (rank 0).  `value` is TFLOP/s over all ranks;
 `roofline` describes the GEMM kernel; `e2e` repeats the step through the
