@@ -426,7 +426,7 @@ def problem_table(problems, out=None):
     return out
 
 
-MAX_DENSE_BATCH = 4  # FP8GEMM_MAX_DENSE_BATCH
+MAX_DENSE_BATCH = 32  # FP8GEMM_MAX_DENSE_BATCH
 
 
 def fp8gemm_dense_batch(problems, stream=None):

@@ -355,12 +355,18 @@ int fp8gemm_grouped_table(const fp8gemm_problem* problems, int num_problems, int
  * problems of prefill size in ONE launch of the 128-row tensor-core GEMM (the
  * grouped GEMM of "bhfrc.com/news/60211" sections 4.2-4.3: one launch over a
  * list of problems, each with its own M, N, K; here the list is on the host
- * and fixed at the call).  Each problem's output tiles are those
- * fp8gemm_dense computes for it on its whole-tile path; the persistent CTAs
- * take the tiles of all problems from one shared sequence -- the problems
- * with the longest K first, then each CTA its next tile when it finishes the
- * last -- so the partial last round of one problem is filled with tiles of
- * the next instead of leaving SMs idle.  A tile's arithmetic and summation
+ * and fixed at the call) -- several layers' GEMMs, or the experts of a MoE
+ * layer whose token counts the host knows (each expert's rows, unpadded, as
+ * one entry).  Each problem's output tiles are those fp8gemm_dense computes
+ * for it on its whole-tile path; the persistent CTAs take the tiles of all
+ * problems from one shared sequence and each CTA its next tile when it
+ * finishes the last, so the partial last round of one problem is filled
+ * with tiles of the next instead of leaving SMs idle.  The sequence runs the
+ * problems with the longest K first; among problems of equal K, the one with
+ * the most tiles, then the one with the fewest, then the second most, ...
+ * (problems with many row blocks reuse their weight tiles from L2 and keep
+ * the tensor cores busy while those with few stream their weights from HBM),
+ * each problem's tiles in the dense form's order.  A tile's arithmetic and summation
  * order do not depend on which CTA takes it, so results are deterministic,
  * and bit-identical to fp8gemm_dense_fmt's where that call takes its
  * whole-tile path with 256-column tiles (N % 256 == 0 or N >= 2048, and at
@@ -382,7 +388,7 @@ int fp8gemm_grouped_table(const fp8gemm_problem* problems, int num_problems, int
  * size, K = 0 or K % 16 != 0), FP8GEMM_ERR_FORMAT, FP8GEMM_ERR_NULL,
  * FP8GEMM_ERR_ALIGN; nothing is enqueued then.
  */
-#define FP8GEMM_MAX_DENSE_BATCH 4
+#define FP8GEMM_MAX_DENSE_BATCH 32
 int fp8gemm_dense_batch(const fp8gemm_problem* problems, int num_problems,
                         fp8gemm_stream_t stream);
 

@@ -183,3 +183,54 @@ def test_batch_prefill_pair_full_size():
         assert np.array_equal(host(b.fp8gemm_dense(*t)), host(D))
     _check(probs, outs, "prefill pair", sample=True)
     assert b.fp8gemm_get_device_status() == b.OK
+
+
+def test_batch_moe_experts_match_the_contiguous_form():
+    """A MoE layer whose token counts the host knows, each expert's unpadded
+    rows as one entry (24 experts, one of them empty: the 32-slot instance):
+    on the real rows bit-identical to fp8gemm_grouped_contiguous over the
+    padded layout (same tile arithmetic), and a sample of every expert
+    against the oracle."""
+    b = _b()
+    E, T, N, K = 24, 2048, 4096, 1024
+    counts = synthetic.zipf_counts(E, T, seed=7)
+    counts[5] = 0
+    X, W, lay = synthetic.contiguous_operands(E, T, N, K, seed=7, counts=counts)
+    A, sA = oquant.quant_1x128_fast(X)
+    Bq = [quant_weights(W[e]) for e in range(E)]
+    B = np.stack([q for q, _ in Bq])
+    sB = np.stack([s for _, s in Bq])
+    tA, tsA, tB, tsB = dev(A), dev(sA), dev(B), dev(sB)
+    Dc = host(b.fp8gemm_grouped_contiguous(tA, tsA, tB, tsB, dev(lay.m_indices)))
+    live = [e for e in range(E) if counts[e] > 0]
+    ents = []
+    for e in live:
+        o, c = int(lay.offsets[e]), int(counts[e])
+        ents.append((tA[o:o + c], tsA[o:o + c], tB[e], tsB[e]))
+    outs = b.fp8gemm_dense_batch(ents)
+    for e, D in zip(live, outs):
+        o, c = int(lay.offsets[e]), int(counts[e])
+        got = host(D)
+        assert np.array_equal(got, Dc[o:o + c]), f"expert {e}"
+        rows, cols = sample_rows_cols(c, N, 6, 40, seed=e)
+        ref = ogemm.gemm_dense_at(A[o:o + c], sA[o:o + c], B[e], sB[e], rows, cols)
+        assert_close(got[rows][:, cols], ref, f"expert {e} ({c} rows)")
+    assert b.fp8gemm_get_device_status() == b.OK
+
+
+def test_batch_many_problems_mixed_k_and_formats():
+    """Nine problems (the 32-slot instance) of three depths of K, ragged sizes
+    and mixed formats: ordered by K, then largest and smallest alternating;
+    each against the oracle."""
+    b = _b()
+    spec = [((300, 512, 1024), ("e4m3", "e4m3")), ((129, 256, 256), ("e5m2", "e4m3")),
+            ((640, 768, 512), ("e4m3", "e4m3")), ((64, 520, 1024), ("e4m3", "e5m2")),
+            ((1100, 1024, 256), ("e4m3", "e4m3")), ((200, 300, 512), ("e5m2", "e5m2")),
+            ((17, 2304, 1024), ("e4m3", "e4m3")), ((400, 256, 256), ("e4m3", "e4m3")),
+            ((257, 1000, 512), ("e4m3", "e4m3"))]
+    probs = [_operands(M, N, K, seed=200 + i, kind="prefill", a_fmt=f[0], b_fmt=f[1])
+             for i, ((M, N, K), f) in enumerate(spec)]
+    entries = [tuple(dev(x) for x in p) + f for p, (_, f) in zip(probs, spec)]
+    outs = b.fp8gemm_dense_batch(entries)
+    _check(probs, outs, "nine problems", fmts=[f for _, f in spec])
+    assert b.fp8gemm_get_device_status() == b.OK
