@@ -111,8 +111,9 @@ struct Tile {
 // dense form.  The persistent CTAs take their first tile by index and every
 // later one from a counter (the next unclaimed tile when a CTA's producer
 // has issued its current tile's loads), so CTAs that finish early take more
-// tiles: with the problems ordered by falling K, the short tiles of the last
-// problems fill the partial last round of the long ones.  The producer hands
+// tiles: with the problems ordered by falling K (among equal K, the largest
+// and the smallest alternating: launch_gemm_tc_batch), the short tiles of the
+// last problems fill the partial last round of the long ones.  The producer hands
 // each tile index to the MMA and promotion warps through a two-slot ring in
 // shared memory; each role maps the index to its tile itself (handing over
 // the mapped fields instead cost the promotion warps a register spill and
