@@ -152,8 +152,9 @@ int finish(cudaError_t e, int nlaunch) {
 // activations of fp8gemm_dense_quant_a at large M -- a separate buffer, so
 // those bytes never land on the counters.
 // Slot kWsTable: the stream-K partials and counters of the problem-table GEMM.
-// Slot kWsBatch: the tile counters of the batched dense GEMM.
-enum { kWsSplitK = 0, kWsQuantA = 1, kWsTable = 2, kWsBatch = 3 };
+// Slot kWsBatch: the tile counters of the batched dense GEMM.  Slot
+// kWsContig: the tile counters and tile order of the contiguous form.
+enum { kWsSplitK = 0, kWsQuantA = 1, kWsTable = 2, kWsBatch = 3, kWsContig = 4 };
 
 int workspace_for(cudaStream_t s, size_t bytes, void** out, int slot = kWsSplitK) {
   int dev = 0;
@@ -460,6 +461,15 @@ int fp8gemm_grouped_contiguous_fmt(const uint8_t* A, const float* sA, int a_fmt,
              M_pad, N, K, E};
   a.a_fmt = a_fmt;
   a.b_fmt = b_fmt;
+  // a wave or more of whole tiles: in expert-segment order, claimed
+  // dynamically (the largest and the smallest experts' tiles side by side)
+  if (const size_t bytes = contig_order_workspace_bytes(c, a)) {
+    void* ws = nullptr;
+    if (int r = workspace_for(stream, bytes, &ws, kWsContig)) return r;
+    int launches = 0;
+    const cudaError_t e = launch_gemm_tc_contiguous_ordered(c, a, ws, bytes, &launches);
+    return finish(e, launches);
+  }
   return run_gemm_tc(c, a);
 }
 

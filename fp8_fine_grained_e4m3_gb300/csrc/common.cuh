@@ -80,6 +80,13 @@ cudaError_t launch_gemm_tc(const LaunchCtx& c, const GemmArgs& a, int* launches)
 // out through `counter` (two zeroed words; each launch leaves them at zero).
 cudaError_t launch_gemm_tc_batch(const LaunchCtx& c, const fp8gemm_problem* p, int count,
                                  unsigned int* counter, int* launches);
+// The contiguous form in expert-segment order (a one-CTA ordering kernel,
+// then the persistent GEMM claiming tiles in that order): the workspace it
+// needs (its counters left at zero by every launch), 0 where the form does
+// not apply -- then launch_gemm_tc takes the call.
+size_t contig_order_workspace_bytes(const LaunchCtx& c, const GemmArgs& a);
+cudaError_t launch_gemm_tc_contiguous_ordered(const LaunchCtx& c, const GemmArgs& a, void* ws,
+                                              size_t ws_bytes, int* launches);
 cudaError_t launch_gemm_small_m(const LaunchCtx& c, const GemmArgs& a, void* workspace,
                                 size_t workspace_bytes);
 size_t small_m_workspace_bytes(int num_sms, int N);

@@ -103,6 +103,7 @@ struct Tile {
   int e;           // expert (0 for dense)
   int p;           // problem of a batched launch (0 otherwise)
   int kb;          // K blocks of that problem (batched launch only)
+  int sb0;         // first sB element of the tile's expert (contiguous order only)
 };
 
 // A batched launch (fp8gemm_dense_batch): independent dense problems, each
@@ -142,6 +143,40 @@ struct BatchParams {
 };
 template <>
 struct BatchParams<0> {};  // the single-problem instances
+// The contiguous form in expert-segment order (kP = -1): its tiles in the
+// order contig_order_kernel wrote, claimed like a batched launch's.
+template <>
+struct BatchParams<-1> {
+  unsigned int* counter;  // [0] claims past the first round, [1] CTAs done, [2] tiles, [3] K blocks
+  const int4* order;      // tile t: first row, first column, expert, expert's first sB element
+};
+
+// Tiles of a launch that claims them dynamically (read after the dependency
+// wait: for the contiguous order, the kernel before this one wrote it).
+template <int P>
+__device__ __forceinline__ int dyn_total(const BatchParams<P>& bp) {
+  if constexpr (P > 0) {
+    return bp.total;
+  } else if constexpr (P < 0) {
+    return int(*reinterpret_cast<volatile const unsigned int*>(bp.counter + 2));
+  } else {
+    return 0;
+  }
+}
+
+// Tile t of the contiguous form in segment order (t < total).
+__device__ __forceinline__ void ordered_tile(const BatchParams<-1>& bp, const GemmArgs& a, int t,
+                                             Tile& tile) {
+  const int4 o = __ldg(bp.order + t);
+  tile.row0 = o.x;
+  tile.n0 = o.y;
+  tile.e = o.z;
+  tile.b_row0 = o.z * a.N + o.y;
+  tile.valid_rows = kBlockM;
+  tile.p = 0;
+  tile.kb = 0;
+  tile.sb0 = o.w;
+}
 
 // Tile t of a batched launch (t < total).
 template <int P>
@@ -280,8 +315,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                    const __grid_constant__ BatchParams<kP> bp) {
   constexpr int BN = Cfg::BN;
   constexpr int kStages = Cfg::kStages;
-  constexpr bool kBatch = kP > 0;
-  static_assert(!(kBatch && kSplit), "batched launches take whole tiles");
+  constexpr bool kBatch = kP > 0;    // independent problems (fp8gemm_dense_batch)
+  constexpr bool kOrdered = kP < 0;  // the contiguous form in segment order
+  constexpr bool kDyn = kP != 0;     // tiles claimed through the counter and the ring
+  static_assert(!(kDyn && kSplit), "dynamic claims take whole tiles");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -317,7 +354,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       mbar_init(&tempty_bar[b], Cfg::kPromoWarps);
     }
     mbar_init(drain_bar, 1);
-    if constexpr (kBatch) {
+    if constexpr (kDyn) {
       for (int i = 0; i < 2; ++i) {
         mbar_init(&ring_full[i], 1);                       // the producer
         mbar_init(&ring_empty[i], 1 + Cfg::kPromoWarps);  // MMA thread + promotion warps
@@ -404,16 +441,23 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      if constexpr (kBatch) {
+      if constexpr (kDyn) {
         // first tile by index, then each from the counter once the current
         // tile's loads are issued; every tile is published on the ring, then
         // the end marker
         uint32_t published = 0;
+        const int total = dyn_total(bp);
         int t = int(blockIdx.x);
         while (ok) {
           Tile tile;
-          const bool have = t < bp.total;
-          if (have) batch_tile(bp, t, BN, tile);
+          const bool have = t < total;
+          if (have) {
+            if constexpr (kBatch) {
+              batch_tile(bp, t, BN, tile);
+            } else {
+              ordered_tile(bp, args, t, tile);
+            }
+          }
           const int slot = int(published & 1);
           if (!mbar_wait(&ring_empty[slot], ((published >> 1) & 1) ^ 1, abort_flag,
                          args.wait_ns)) {
@@ -424,9 +468,15 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           mbar_arrive(&ring_full[slot]);
           ++published;
           if (!have) break;
-          const CUtensorMap* mA = &bp.a[tile.p];
-          const CUtensorMap* mB = &bp.b[tile.p];
-          for (int kb = 0; kb < tile.kb; ++kb, ++it) {
+          const CUtensorMap* mA = &tmA;
+          const CUtensorMap* mB = &tmB;
+          int kb_end = kb1;
+          if constexpr (kBatch) {
+            mA = &bp.a[tile.p];
+            mB = &bp.b[tile.p];
+            kb_end = tile.kb;
+          }
+          for (int kb = 0; kb < kb_end; ++kb, ++it) {
             const int s = it % kStages;
             const uint32_t ph = (it / kStages) & 1;
             if (!mbar_wait(&empty_bar[s], ph ^ 1, abort_flag, args.wait_ns)) {
@@ -441,7 +491,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           if (ok) t = int(gridDim.x) + int(atomicAdd(bp.counter, 1u));
         }
       }
-      for (int t = first_tile(t_begin); !kBatch && t < end_tile(t_end) && ok; t += tile_step()) {
+      for (int t = first_tile(t_begin); !kDyn && t < end_tile(t_end) && ok; t += tile_step()) {
         Tile tile;
         if (!sched.get(t, BN, tile)) continue;
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
@@ -471,9 +521,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       const uint32_t b_base = smem_addr(smB);
       uint32_t it = 0;
       bool ok = true;
-      for (int t = kBatch ? ring_index(false) : first_tile(t_begin);
-           (kBatch ? t >= 0 : t < end_tile(t_end)) && ok;
-           t = kBatch ? ring_index(false) : t + tile_step()) {
+      for (int t = kDyn ? ring_index(false) : first_tile(t_begin);
+           (kDyn ? t >= 0 : t < end_tile(t_end)) && ok;
+           t = kDyn ? ring_index(false) : t + tile_step()) {
         Tile tile;
         uint32_t idesc_t = idesc;
         int kb_end = kb1;
@@ -482,6 +532,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           const int f = bp.prob[tile.p].fmts;
           idesc_t = idesc_f8_f32(kBlockM, BN, uint32_t(f & 0xff), uint32_t(f >> 8));
           kb_end = tile.kb;
+        } else if constexpr (kOrdered) {
+          ordered_tile(bp, args, t, tile);
         } else if (!sched.get(t, BN, tile)) {
           continue;
         }
@@ -523,12 +575,14 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     uint32_t it = 0;
     uint32_t n_stores = 0;  // TMA stores this warp has issued (alternates the boxes)
     bool ok = true;
-    for (int t = kBatch ? ring_index(true) : first_tile(t_begin);
-         (kBatch ? t >= 0 : t < end_tile(t_end)) && ok;
-         t = kBatch ? ring_index(true) : t + tile_step()) {
+    for (int t = kDyn ? ring_index(true) : first_tile(t_begin);
+         (kDyn ? t >= 0 : t < end_tile(t_end)) && ok;
+         t = kDyn ? ring_index(true) : t + tile_step()) {
       Tile tile;
       if constexpr (kBatch) {
         batch_tile(bp, t, BN, tile);
+      } else if constexpr (kOrdered) {
+        ordered_tile(bp, args, t, tile);
       } else if (!sched.get(t, BN, tile)) {
         continue;
       }
@@ -544,6 +598,15 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         sa_ptr = pr.sA + size_t(tile.row0 + row) * tile.kb;
         sb_ptr = pr.sB + size_t(col0 / kBlockK) * tile.kb;
         kb_end = tile.kb;
+      } else if constexpr (kOrdered) {
+        // the K block count read per tile from the workspace, and the
+        // expert's scale offset from the order: kept in registers through
+        // the tile loop instead, they made ptxas spill here
+        const int kbo = int(*reinterpret_cast<volatile const unsigned int*>(bp.counter + 3));
+        cols_ok = col0 < args.N;
+        sa_ptr = args.sA + size_t(tile.row0 + row) * kbo;
+        sb_ptr = args.sB + tile.sb0 + size_t(col0 / kBlockK) * kbo;
+        kb_end = kbo;
       } else {
         cols_ok = col0 < args.N;
         sa_ptr = args.sA + size_t(tile.row0 + row) * Kb;
@@ -744,7 +807,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   }
 
   __syncthreads();
-  if constexpr (kBatch) {
+  if constexpr (kDyn) {
     // every claim of this CTA precedes its count; the last CTA to count
     // leaves both counters at zero for the next launch (which reads them
     // only after this grid has completed)
@@ -759,6 +822,150 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   if (warp == Cfg::kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+
+// ----------------------------------------- contiguous form in segment order
+// One CTA orders the contiguous form's tiles before the GEMM runs them: it
+// reads the expert of each 128-row block (m_indices of its first row, as the
+// GEMM does), takes each maximal run of blocks of one expert as a segment,
+// and lays the segments out largest, smallest, second largest, ... (more
+// than kOrderMaxSegs segments: in block order), each segment's tiles in the
+// dense form's grouped rasterisation over its own blocks.  Blocks of padding
+// (index -1) get no tile; an index >= E sets the status word and its block
+// gets no tile.  Tile t of the order: (first row, first column, expert,
+// the expert's first sB element).
+constexpr int kOrderThreads = 1024;
+constexpr int kOrderMaxBlocks = 2048;  // M blocks this ordering takes (larger: block order kernel)
+constexpr int kOrderMaxSegs = 256;     // segments it reorders by size
+
+// Exclusive prefix sum over the CTA of one value per thread; *total gets the sum.
+__device__ __forceinline__ int cta_exclusive_scan(int v, int* warp_sums, int* total) {
+  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+  int x = v;
+#pragma unroll
+  for (int d = 1; d < 32; d *= 2) {
+    const int y = __shfl_up_sync(0xffffffffu, x, d);
+    if (lane >= d) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < kOrderThreads / 32 ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int d = 1; d < 32; d *= 2) {
+      const int y = __shfl_up_sync(0xffffffffu, w, d);
+      if (lane >= d) w += y;
+    }
+    warp_sums[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  const int before = (warp > 0 ? warp_sums[warp - 1] : 0) + x - v;
+  *total = warp_sums[kOrderThreads / 32 - 1];
+  __syncthreads();
+  return before;
+}
+
+__global__ void __launch_bounds__(kOrderThreads, 1)
+    contig_order_kernel(const int32_t* m_indices, int num_m, int E, int num_n, int BN, int Nb,
+                        int Kb, int4* order, unsigned int* counter, int* status) {
+  __shared__ int blk[kOrderMaxBlocks];       // expert of each block, -1: no tile
+  __shared__ int seg_first[kOrderMaxBlocks];
+  __shared__ int seg_len[kOrderMaxBlocks];
+  __shared__ int pos_seg[kOrderMaxBlocks];   // segment at each position of the order
+  __shared__ int pos_tile0[kOrderMaxBlocks]; // its first tile
+  __shared__ int warp_sums[32];
+  const int tid = threadIdx.x;
+  // m_indices may come from the kernel before this one; the GEMM behind may
+  // start its prologue now (it reads the order only after this grid ends)
+  griddep_wait();
+  griddep_launch_dependents();
+  for (int mb = tid; mb < num_m; mb += kOrderThreads) {
+    int e = __ldg(m_indices + size_t(mb) * kBlockM);
+    if (e >= E) {
+      raise_status(status, FP8GEMM_ERR_DEVICE_STATUS);
+      e = -1;
+    }
+    blk[mb] = e < 0 ? -1 : e;
+  }
+  __syncthreads();
+  // segment starts: a block with work whose predecessor holds another expert
+  constexpr int kPer = kOrderMaxBlocks / kOrderThreads;
+  auto is_start = [&](int mb) {
+    return mb < num_m && blk[mb] >= 0 && (mb == 0 || blk[mb - 1] != blk[mb]);
+  };
+  int mine = 0;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) mine += is_start(tid * kPer + j) ? 1 : 0;
+  int S = 0;
+  int sid = cta_exclusive_scan(mine, warp_sums, &S);
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int mb = tid * kPer + j;
+    if (is_start(mb)) {
+      int len = 1;
+      while (mb + len < num_m && blk[mb + len] == blk[mb]) ++len;
+      seg_first[sid] = mb;
+      seg_len[sid] = len;
+      ++sid;
+    }
+  }
+  __syncthreads();
+  // positions: by falling length (ties: segment order), the largest and the
+  // smallest alternating
+  for (int q = tid; q < S; q += kOrderThreads) {
+    int pos = q;
+    if (S <= kOrderMaxSegs) {
+      const int L = seg_len[q];
+      int rank = 0;
+      for (int u = 0; u < S; ++u) {
+        const int Lu = seg_len[u];
+        rank += (Lu > L || (Lu == L && u < q)) ? 1 : 0;
+      }
+      const int half = (S + 1) / 2;
+      pos = rank < half ? 2 * rank : 2 * (S - 1 - rank) + 1;
+    }
+    pos_seg[pos] = q;
+  }
+  __syncthreads();
+  int tiles_mine[kPer];
+  int sum_mine = 0;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int pos = tid * kPer + j;
+    tiles_mine[j] = pos < S ? seg_len[pos_seg[pos]] * num_n : 0;
+    sum_mine += tiles_mine[j];
+  }
+  int total = 0;
+  int first = cta_exclusive_scan(sum_mine, warp_sums, &total);
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int pos = tid * kPer + j;
+    if (pos < S) pos_tile0[pos] = first;
+    first += tiles_mine[j];
+  }
+  __syncthreads();
+  for (int t = tid; t < total; t += kOrderThreads) {
+    int lo = 0, hi = S - 1;  // the last position whose first tile is <= t
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) / 2;
+      if (pos_tile0[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    const int q = pos_seg[lo];
+    const int len = seg_len[q], mb0 = seg_first[q];
+    const int u = t - pos_tile0[lo];
+    const int per_group = kGroupM * num_n;
+    const int g = u / per_group;
+    const int first_m = g * kGroupM;
+    const int gs = min(kGroupM, len - first_m);
+    const int r = u - g * per_group;
+    order[t] = make_int4((mb0 + first_m + r % gs) * kBlockM, (r / gs) * BN, blk[mb0],
+                         blk[mb0] * Nb * Kb);
+  }
+  if (tid == 0) {
+    counter[2] = unsigned(total);
+    counter[3] = unsigned(Kb);
   }
 }
 
@@ -964,6 +1171,70 @@ cudaError_t launch_batch(const LaunchCtx& c, const fp8gemm_problem* p, const int
 }
 
 }  // namespace
+
+size_t contig_order_workspace_bytes(const LaunchCtx& c, const GemmArgs& a) {
+  using Cfg = TcCfg<256, 4>;
+  const long long num_m = a.M / kBlockM, num_n = ceil_div(a.N, Cfg::BN);
+  const bool wide = (a.N % 256 == 0) || a.N >= 2048;  // launch_gemm_tc's BN = 256 instance
+  const long long sb_elems = (long long)a.E * ceil_div(a.N, kBlockK) * ceil_div(a.K, kBlockK);
+  if (a.mode != GemmMode::kContiguous || !wide || num_m > kOrderMaxBlocks ||
+      num_m * num_n < c.num_sms || ceil_div(a.K, kBlockK) < 2 || sb_elems > 0x7fffffffLL)
+    return 0;
+  return 16 + size_t(num_m * num_n) * sizeof(int4);
+}
+
+cudaError_t launch_gemm_tc_contiguous_ordered(const LaunchCtx& c, const GemmArgs& a0, void* ws,
+                                              size_t ws_bytes, int* launches) {
+  using Cfg = TcCfg<256, 4>;
+  *launches = 0;
+  const size_t need = contig_order_workspace_bytes(c, a0);
+  if (need == 0 || ws_bytes < need) return cudaErrorInvalidValue;
+  GemmArgs a = a0;
+  a.wait_ns = wait_limit_ns();
+  const int num_m = a.M / kBlockM, num_n = ceil_div(a.N, Cfg::BN);
+  CUtensorMap tmA, tmB, tmD;
+  if (!make_tmap_u8_sw128(&tmA, a.A, uint64_t(a.M), a.K, kBlockM)) return cudaErrorInvalidValue;
+  if (!make_tmap_u8_sw128(&tmB, a.B, uint64_t(a.E) * a.N, a.K, Cfg::BN))
+    return cudaErrorInvalidValue;
+  memset(&tmD, 0, sizeof(tmD));
+  a.d_tma = make_tmap_bf16_sw64(&tmD, a.D, uint64_t(a.M), uint64_t(a.N), 32) ? 1 : 0;
+  if (cudaError_t e = set_smem_attr<Cfg, false, -1>()) return e;
+  unsigned int* counter = static_cast<unsigned int*>(ws);
+  int4* order = reinterpret_cast<int4*>(static_cast<char*>(ws) + 16);
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  // the order, then the GEMM, each as a programmatic dependent of the kernel
+  // before it (the GEMM's prologue overlaps the ordering)
+  cudaLaunchConfig_t cfg0 = {};
+  cfg0.gridDim = dim3(1);
+  cfg0.blockDim = dim3(kOrderThreads);
+  cfg0.stream = c.stream;
+  cfg0.attrs = &attr;
+  cfg0.numAttrs = 1;
+  if (cudaError_t e = cudaLaunchKernelEx(&cfg0, contig_order_kernel, a.group_info, num_m, a.E,
+                                         num_n, Cfg::BN, ceil_div(a.N, kBlockK),
+                                         ceil_div(a.K, kBlockK), order, counter, c.status))
+    return e;
+  *launches = 1;
+  const long long bound = (long long)num_m * num_n;  // tiles, padding blocks included
+  const int grid = int(bound < c.num_sms ? bound : c.num_sms);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(grid));
+  cfg.blockDim = dim3(Cfg::kThreads);
+  cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+  cfg.stream = c.stream;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  BatchParams<-1> bp;
+  bp.counter = counter;
+  bp.order = order;
+  if (cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<Cfg, false, -1>, tmA, tmB, tmD, a,
+                                         c.status, bp))
+    return e;
+  *launches = 2;
+  return cudaSuccess;
+}
 
 cudaError_t launch_gemm_tc_batch(const LaunchCtx& c, const fp8gemm_problem* p, int count,
                                  unsigned int* counter, int* launches) {
