@@ -47,7 +47,9 @@
  *    sums through a per-(device, stream) workspace that the library allocates
  *    with cudaMalloc on the first such call on that stream (about 10 MB, kept
  *    until released or process exit) and zeroes on that stream; fp8gemm_dense_quant_a at
- *    M > 64 without Q/sA keeps its quantised A in a second per-stream buffer.
+ *    M > 64 without Q/sA keeps its quantised A in a second per-stream buffer,
+ *    and fp8gemm_dense_batch and the ordered contiguous form their tile
+ *    counters (and order) in small per-stream buffers.
  *    Such a first call must therefore not happen during CUDA graph capture.
  *    Calls on different streams never share a workspace.  The reduction
  *    order is fixed, so results are deterministic.  A caller that retires a
@@ -267,6 +269,19 @@ int fp8gemm_dense_quant_a_ex(const float* X, uint8_t* Q, float* sA, const uint8_
  *   (segments padded to 128 rows, padding at each segment's end).  Only the
  *   first row's index of each block is read; a block whose first index is -1
  *   is skipped; an index >= E sets FP8GEMM_ERR_DEVICE_STATUS.
+ *
+ * When the tiles (M_pad/128 x ceil(N/256)) make at least a wave of the SMs,
+ * with N % 256 == 0 or N >= 2048, K > 128, M_pad <= 262144 and
+ * E * ceil(N/128) * ceil(K/128) < 2^31, the call is two launches: a one-CTA
+ * kernel that orders the tiles by expert segment (the experts with the most
+ * and the fewest blocks alternating, so the tiles that stream their weights
+ * from HBM run beside those that reuse them from L2), then the GEMM taking
+ * its tiles in that order.  The order and two tile counters live in a
+ * per-(device, stream) workspace of 16 + 16 * tiles bytes that the library
+ * allocates and zeroes on the first such call on the stream (not during
+ * stream capture; see the conventions above) and that every launch leaves
+ * ready for the next.  Results do not depend on the order: each tile's
+ * arithmetic is the same.
  */
 int fp8gemm_grouped_contiguous(const uint8_t* A, const float* sA, const uint8_t* B,
                                const float* sB, const int32_t* m_indices, void* D,
@@ -451,8 +466,10 @@ uint64_t fp8gemm_num_kernel_launches(void);
 
 /*
  * fp8gemm_release_workspaces -- free every library-owned workspace of
- * `stream` on the current device (the split-K buffer of the decode path and
- * the quantised-activation buffer of fp8gemm_dense_quant_a).  It first
+ * `stream` on the current device (the split-K buffer of the decode path, the
+ * quantised-activation buffer of fp8gemm_dense_quant_a, the problem table's
+ * partials, and the tile counters and order of fp8gemm_dense_batch and of
+ * the ordered contiguous form).  It first
  * synchronises `stream`, since work enqueued there may still use them; the
  * next call that needs a workspace on that stream allocates it again.  Call
  * it before cudaStreamDestroy for streams that are retired: a stream handle
