@@ -55,3 +55,45 @@ def test_workspaces_follow_streams_and_are_released():
     b.fp8gemm_release_workspaces(streams[0])
     assert b.workspace_bytes() == base
     assert b.fp8gemm_get_device_status() == b.OK
+
+
+def test_tile_counter_workspaces_are_released():
+    """The batched launch's counters and the ordered contiguous form's
+    counters and order are per-stream workspaces too: released with the
+    stream's other buffers, and allocated again (zeroed) by the next call,
+    which is still correct."""
+    import numpy as np
+    import torch
+
+    from fp8_fine_grained_e4m3_gb300 import binding as b
+    from fp8_fine_grained_e4m3_gb300 import synthetic
+    from tests.gpu_helpers import quant_weights
+    shapes = [(1300, 4000, 640), (300, 520, 1024)]
+    probs = [quantised_dense(M, N, K, "prefill", seed=70 + i) for i, (M, N, K) in enumerate(shapes)]
+    ops = [tuple(dev(x) for x in p) for p in probs]
+    refs = [ogemm.gemm_dense(*p) for p in probs]
+    E, N, K = 10, 4096, 512
+    counts = synthetic.zipf_counts(E, 2500, seed=71)
+    X, W, lay = synthetic.contiguous_operands(E, 2500, N, K, seed=71, counts=counts)
+    Ac, sAc = oquant.quant_1x128_fast(X)
+    Bq = [quant_weights(W[e]) for e in range(E)]
+    Bc = np.stack([q for q, _ in Bq])
+    sBc = np.stack([s for _, s in Bq])
+    cops = (dev(Ac), dev(sAc), dev(Bc), dev(sBc), dev(lay.m_indices))
+    cref = ogemm.gemm_contiguous(Ac, sAc, Bc, sBc, lay.m_indices)
+
+    torch.cuda.synchronize()
+    base = b.workspace_bytes()
+    s = torch.cuda.Stream()
+    for rep in range(2):
+        with torch.cuda.stream(s):
+            outs = b.fp8gemm_dense_batch(ops)
+            Dc = b.fp8gemm_grouped_contiguous(*cops)
+        s.synchronize()
+        for D, r in zip(outs, refs):
+            assert_close(host(D), r, f"batch, pass {rep}")
+        assert_close(host(Dc), cref, f"ordered contiguous, pass {rep}")
+        assert b.workspace_bytes() > base
+        b.fp8gemm_release_workspaces(s)
+        assert b.workspace_bytes() == base
+    assert b.fp8gemm_get_device_status() == b.OK
