@@ -46,6 +46,13 @@
 // news/5092" section 3.2: size the work to the SM count).  The masked form
 // enumerates only tiles that hold valid rows, so no CTA idles on an empty
 // expert ("lpnh.cn/news/2822121" section 5.2: skip empty blocks).
+//
+// Dynamic tile claims: two more instances hand tiles out from a counter
+// instead of by CTA index -- a batched launch of independent dense problems
+// (kP > 0, fp8gemm_dense_batch) and the contiguous form in expert-segment
+// order (kP < 0, after contig_order_kernel) -- so that CTAs which finish
+// early take more tiles ("bhfrc.com/news/60211" sections 4.2-4.3: one launch
+// over a list of problems).
 #include <cstring>
 
 #include "common.cuh"
