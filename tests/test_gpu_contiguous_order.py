@@ -151,3 +151,23 @@ def test_ordered_contiguous_chains_and_graph_replay():
         torch.cuda.synchronize()
         assert np.array_equal(host(D)[real], ref[real]), f"graph replay {rep}"
     assert b.fp8gemm_get_device_status() == b.OK
+
+
+def test_ordered_contiguous_many_segments_keep_block_order():
+    """More than 256 expert segments: the ordering kernel keeps them in block
+    order (no ranking) and the result is still every row against the oracle
+    (300 experts of 1-9 tokens, one 128-row block each)."""
+    b = _b()
+    E, N, K = 300, 512, 256
+    counts = 1 + np.random.default_rng(21).integers(0, 9, E)
+    mi = _layout(counts)
+    A, sA = _rows(mi, K, seed=22)
+    W = synthetic.dense_operands(8, N, K, kind="normal", seed=23)[1]
+    Bq = [quant_weights(np.roll(W, e, axis=1)) for e in range(E)]
+    B = np.stack([q for q, _ in Bq])
+    sB = np.stack([s for _, s in Bq])
+    l0 = b.num_kernel_launches()
+    got = host(b.fp8gemm_grouped_contiguous(dev(A), dev(sA), dev(B), dev(sB), dev(mi)))
+    assert b.num_kernel_launches() - l0 == 2
+    assert_close(got, ogemm.gemm_contiguous(A, sA, B, sB, mi), "300 segments")
+    assert b.fp8gemm_get_device_status() == b.OK
