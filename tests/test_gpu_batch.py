@@ -234,3 +234,20 @@ def test_batch_many_problems_mixed_k_and_formats():
     outs = b.fp8gemm_dense_batch(entries)
     _check(probs, outs, "nine problems", fmts=[f for _, f in spec])
     assert b.fp8gemm_get_device_status() == b.OK
+
+
+def test_batch_full_32_problems():
+    """Exactly FP8GEMM_MAX_DENSE_BATCH problems (every parameter slot of the
+    32-slot instance in use): random sizes, two depths of K, against the
+    oracle; one more entry is refused on the host."""
+    b = _b()
+    g = np.random.default_rng(33)
+    shapes = [(int(g.integers(1, 300)), int(g.choice([256, 512, 520])), int(g.choice([128, 256])))
+              for _ in range(b.MAX_DENSE_BATCH)]
+    probs = [_operands(M, N, K, seed=300 + i) for i, (M, N, K) in enumerate(shapes)]
+    tens = [tuple(dev(x) for x in p) for p in probs]
+    outs = b.fp8gemm_dense_batch(tens)
+    _check(probs, outs, "32 problems")
+    with pytest.raises(ValueError, match="at most"):
+        b.fp8gemm_dense_batch(tens + tens[:1])
+    assert b.fp8gemm_get_device_status() == b.OK
